@@ -1,0 +1,10 @@
+"""fp64 CPU oracle for the BackLite attention hot path.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``, never by the library.  It shares no
+code with the CUDA path.
+
+* ``attention``  -- exact forward, per-tile LSE statistics, masked backward.
+* ``mask_spec``  -- the canonical tile-selection rule (mask_from_stats).
+"""
+from . import attention, mask_spec  # noqa: F401
