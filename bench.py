@@ -1,0 +1,411 @@
+"""Benchmark of the BackLite hot path on one GB300 (or N, one process each).
+
+One step = exact forward with tile statistics -> mask_from_stats -> block-
+sparse backward, on the video-DiT-shaped workload (B=1, H=Hk=40, n=32760 =
+21x30x52 latent grid, d=128, 128x128 tiles, negl_prob=0.05, clustered
+synthetic inputs, seed 0).  Inputs are resident in HBM and larger than the
+129 MB L2 (Q alone is 335 MB), so no flush is needed between steps.
+
+Printed JSON line (rank 0): ``value`` = attention-backward milliseconds per
+step (mask_from_stats + backward, CUDA events on the launch stream, max over
+ranks), with dense-equivalent TFLOP/s, skipped-tile fraction and the
+fraction of the measured bf16 tensor peak on the computed tiles beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (query tiles of a few heads) and scales it to the full
+backward in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn bwd ms + dense-equiv TFLOP/s at n=32k,d=128; skip %; % bf16 tensor peak"
+WORKLOAD = "video_n32760_d128"
+NEGL = 0.05
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained"),
+                "hbm": d["hbm_gbs"], "src": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.rows = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=5).stdout.strip()
+                if out:
+                    self.rows.append([x.strip() for x in out.split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def _smi_id(dev):
+    """nvidia-smi --id for a torch device: its UUID (independent of
+    CUDA_VISIBLE_DEVICES renumbering), else the visible index."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in vis.split(",") if p.strip()]
+    idx = dev.index or 0
+    return parts[idx].strip() if idx < len(parts) else str(idx)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_reference_sample(w, q, k, v, go, budget_s=15.0, max_tiles=256):
+    """Time the oracle's backward for whole query tiles of the workload.
+
+    For each sampled (head, query tile) the oracle forms the tile's exact
+    forward rows (LSE and tile statistics against every key), applies the
+    selection rule to that tile's row of key tiles and computes G_Q for the
+    tile's rows with the masked backward.  Returns (ms for the full backward
+    extrapolated over all B*H*T_r query tiles, description, tiles, seconds).
+    """
+    import numpy as np
+
+    from oracle import attention as A
+    from oracle import mask_spec as M
+
+    rng = np.random.default_rng(1)
+    T_r = w.T_r
+    t0 = time.perf_counter()
+    done = 0
+    qn = q.float().numpy()
+    kn = k.float().numpy()
+    vn = v.float().numpy()
+    gn = go.float().numpy()
+    while done < max_tiles and time.perf_counter() - t0 < budget_s:
+        h = int(rng.integers(w.H))
+        hk = h // (w.H // w.Hk)
+        i = int(rng.integers(T_r))
+        rows = np.arange(i * w.block_q, min(w.n, (i + 1) * w.block_q))
+        qh = qn[0, :, h].astype(np.float64)
+        kh = kn[0, :, hk].astype(np.float64)
+        vh = vn[0, :, hk].astype(np.float64)
+        o_r, l_r, st_r = A.forward_head(qh, kh, vh, w.scale, rows=rows, block_k=w.block_k)
+        d = M.tile_weights(st_r.astype(np.float32), l_r.astype(np.float32), len(rows), w.block_q)
+        act, _ = M.select_row(d[0], M.threshold(NEGL))
+        tm = np.zeros((T_r, w.T_c), dtype=np.uint8)
+        tm[i] = act
+        o_full = np.zeros_like(qh)
+        o_full[rows] = o_r
+        lse_full = np.zeros(w.n)
+        lse_full[rows] = l_r
+        A.backward_head(qh, kh, vh, o_full, gn[0, :, h].astype(np.float64), lse_full, w.scale,
+                        tm, w.block_q, w.block_k, rows=rows)
+        done += 1
+    el = time.perf_counter() - t0
+    total_tiles = w.B * w.H * T_r
+    ms_full = el / done * total_tiles * 1e3
+    desc = (f"{done} random (head, query tile) pairs of {total_tiles}: exact forward rows, "
+            f"tile stats, selection and G_Q in fp64, extrapolated to the full backward")
+    return ms_full, desc, done, el
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from block_sparse_attention_fwd_gb300 import inputs
+    w = inputs.WORKLOADS[WORKLOAD]
+    q, k, v, go = inputs.generate(w, seed=0)
+    cores = os.cpu_count()
+    vals = []
+    for s in range(args.warmup + args.steps):
+        ms, desc, tiles, el = cpu_reference_sample(w, q, k, v, go, budget_s=args.ref_budget,
+                                                   max_tiles=args.ref_tiles)
+        if s >= args.warmup:
+            vals.append(ms)
+    val = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "ms",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": val,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "B": w.B, "n": w.n, "H": w.H,
+                                            "Hk": w.Hk, "d": w.d, "tiles": "128x128",
+                                            "negl_prob": NEGL},
+            "cpu_baseline": {"value": val, "unit": "ms", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": val, "unit": "ms", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    from block_sparse_attention_fwd_gb300 import _lib, build, inputs
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = inputs.WORKLOADS[args.workload]
+    negl = args.negl
+    # weak scaling: every rank runs its own independent problem (seed = rank)
+    q, k, v, go = inputs.generate(w, seed=rank)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    T_r, T_c = _lib.tiles(shape)
+    qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.n), dtype=torch.float32, device=dev)
+    stats = torch.empty((w.B, w.H, T_c, T_r * w.block_q), dtype=torch.float32, device=dev)
+    lists = _lib.alloc_lists(shape, dev)
+    g_q, g_k, g_v = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        _lib.attn_fwd(shape, qd, kd, vd, w.scale, o, lse, stats)
+        if ev:
+            ev[1].record(stream)
+        _lib.mask_from_stats(shape, stats, lse, negl, lists)
+        if ev:
+            ev[2].record(stream)
+        _lib.attn_bwd(shape, qd, kd, vd, o, god, lse, w.scale, lists, g_q, g_k, g_v, wsb)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if _lib.bwd_check_status(shape, wsb) != 0:
+        raise RuntimeError("backward reported corrupt tile lists")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(_smi_id(dev)) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    mask_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    bwd_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    attn_bwd = [m + b for m, b in zip(mask_ms, bwd_ms)]
+    step_ms = total_ms / args.steps
+    vals = torch.tensor([statistics.mean(attn_bwd), step_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+    attn_bwd_ms, step_ms = float(vals[0]), float(vals[1])
+
+    # sparsity of this step's mask
+    mask = lists["mask"]
+    n_active = int(mask.sum(dtype=torch.int64).item())
+    n_tiles = mask.numel()
+    skip = 1.0 - n_active / n_tiles
+
+    # dense backward at the same shape (lists = NULL), same timing method
+    dense_ms = []
+    for _ in range(args.dense_iters):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        _lib.attn_bwd(shape, qd, kd, vd, o, god, lse, w.scale, None, g_q, g_k, g_v, wsb)
+        b.record(stream)
+        torch.cuda.synchronize()
+        dense_ms.append(a.elapsed_time(b))
+    # restore the sparse gradients (not needed for timing; keeps buffers meaningful)
+
+    pk = _peaks()
+    dense_flop = w.dense_bwd_flop()
+    # computed-tile work: 10*Br*Bc*d per active (head, q tile, k tile) triple,
+    # counting only the valid rows/keys of ragged edge tiles
+    computed_flop = _active_flop(mask, w)
+    bwd_only = statistics.mean(bwd_ms)
+    achieved_tf = computed_flop / (bwd_only * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": attn_bwd_ms, "unit": "ms", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded clustered generator, video-grid clusters)",
+        "config": {"workload": args.workload, "B": w.B, "n": w.n, "H": w.H, "Hk": w.Hk,
+                   "d": w.d, "tiles": f"{w.block_q}x{w.block_k}", "negl_prob": negl,
+                   "l2": "inputs larger than L2 (no flush)"},
+        "fwd_ms": statistics.mean(fwd_ms), "mask_ms": statistics.mean(mask_ms),
+        "bwd_kernels_ms": bwd_only,
+        "dense_bwd_ms": statistics.median(dense_ms) if dense_ms else None,
+        "dense_equiv_tflops": dense_flop / (attn_bwd_ms * 1e-3) / 1e12,
+        "skip_frac": skip,
+        "frac_bf16_peak_computed_tiles": achieved_tf / pk["bf16"],
+        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16"],
+                     "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16"], "traffic": None,
+                     "kernel": "bl_attn_bwd (all its launches; dK/dV pass dominant)",
+                     "peak_src": pk["src"]},
+        "gpu_launches": 6 * args.steps,
+    }
+    clk_s = clk.summary()
+    line["clocks"] = clk_s
+
+    if not args.no_e2e:
+        line["e2e"] = _e2e(args, w, shape, q, k, v, go, negl, dev)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        ms_cpu, desc, tiles, el = cpu_reference_sample(w, q, k, v, go, budget_s=args.ref_budget,
+                                                       max_tiles=args.ref_tiles)
+        line["cpu_baseline"] = {"value": ms_cpu, "unit": "ms", "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def _active_flop(mask, w):
+    import torch
+    T_r, T_c = mask.shape[2], mask.shape[3]
+    rows = torch.full((T_r,), w.block_q, dtype=torch.float64)
+    rows[-1] = w.n - (T_r - 1) * w.block_q
+    cols = torch.full((T_c,), w.block_k, dtype=torch.float64)
+    cols[-1] = w.n - (T_c - 1) * w.block_k
+    m = mask.to("cpu", torch.float64)
+    return float(10.0 * w.d * torch.einsum("bhij,i,j->", m, rows, cols))
+
+
+def _e2e(args, w, shape, q, k, v, go, negl, dev):
+    """Same step through the public API with host buffers: pinned H2D copies of
+    Q, K, V, G_O and D2H copies of G_Q, G_K, G_V inside the timed region."""
+    import torch
+
+    from block_sparse_attention_fwd_gb300 import _lib
+    hq, hk, hv, hg = (x.pin_memory() for x in (q, k, v, go))
+    outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q, k, v)]
+    dq, dk, dv, dg = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q, k, v, go))
+    o = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, w.n), dtype=torch.float32, device=dev)
+    T_r, T_c = _lib.tiles(shape)
+    stats = torch.empty((w.B, w.H, T_c, T_r * w.block_q), dtype=torch.float32, device=dev)
+    lists = _lib.alloc_lists(shape, dev)
+    gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dg, hg)):
+            dst.copy_(src, non_blocking=True)
+        _lib.attn_fwd(shape, dq, dk, dv, w.scale, o, lse, stats)
+        _lib.mask_from_stats(shape, stats, lse, negl, lists)
+        _lib.attn_bwd(shape, dq, dk, dv, o, dg, lse, w.scale, lists, gq, gk, gv, wsb)
+        for dst, src in zip(outs, (gq, gk, gv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 5))
+    a.record(stream)
+    for _ in range(n):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, go))
+    d2h = sum(x.numel() * x.element_size() for x in (gq, gk, gv))
+    return {"value": a.elapsed_time(b) / n, "unit": "ms", "what": "H2D inputs + fwd + mask + "
+            "bwd + D2H gradients, ms per step", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--negl", type=float, default=NEGL)
+    ap.add_argument("--dense-iters", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=15.0)
+    ap.add_argument("--ref-tiles", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

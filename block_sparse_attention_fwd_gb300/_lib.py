@@ -1,0 +1,193 @@
+"""ctypes binding of libbl_attn.so (argument marshalling only).
+
+Every function takes torch CUDA tensors, checks dtype/shape/contiguity and
+passes raw device pointers plus the current CUDA stream to the C ABI
+declared in ``include/bl_attn.h``.  There is no fallback: if the library is
+missing or a call fails, a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbl_attn.so")
+
+BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "BL_ERR_CUDA",
+             4: "BL_ERR_WORKSPACE", 5: "BL_ERR_CORRUPT_LISTS", 6: "BL_ERR_TIMEOUT"}
+
+# Every symbol include/bl_attn.h declares (checked by the CPU test suite).
+EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
+           "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("n", ctypes.c_int), ("H", ctypes.c_int),
+                ("Hk", ctypes.c_int), ("d", ctypes.c_int), ("block_q", ctypes.c_int),
+                ("block_k", ctypes.c_int)]
+
+
+class Lists(ctypes.Structure):
+    _fields_ = [("mask", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p),
+                ("kv_cnt", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
+                ("q_cnt", ctypes.c_void_p), ("nan_count", ctypes.c_void_p)]
+
+
+class BLError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {BL_STATUS.get(code, code)}")
+
+
+_lib = None
+
+
+def load():
+    """Load libbl_attn.so once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m block_sparse_attention_fwd_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, S, F, D, Z = ctypes.c_void_p, ctypes.POINTER(Shape), ctypes.c_float, ctypes.c_double, ctypes.c_size_t
+    lib.bl_tile_stats_elems.argtypes = [S]
+    lib.bl_tile_stats_elems.restype = Z
+    lib.bl_bwd_workspace_bytes.argtypes = [S]
+    lib.bl_bwd_workspace_bytes.restype = Z
+    lib.bl_attn_fwd.argtypes = [S, P, P, P, F, P, P, P, P]
+    lib.bl_attn_fwd.restype = ctypes.c_int
+    lib.bl_mask_from_stats.argtypes = [S, P, P, D, ctypes.POINTER(Lists), P]
+    lib.bl_mask_from_stats.restype = ctypes.c_int
+    lib.bl_attn_bwd.argtypes = [S, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P, P, Z, P]
+    lib.bl_attn_bwd.restype = ctypes.c_int
+    lib.bl_bwd_check_status.argtypes = [S, P, P]
+    lib.bl_bwd_check_status.restype = ctypes.c_int
+    lib.bl_status_string.argtypes = [ctypes.c_int]
+    lib.bl_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != 0:
+        raise BLError(fn, code)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_shape(B, n, H, Hk, d, block_q, block_k) -> Shape:
+    return Shape(B, n, H, Hk, d, block_q, block_k)
+
+
+def tiles(shape: Shape):
+    T_r = -(-shape.n // shape.block_q)
+    T_c = -(-shape.n // shape.block_k)
+    return T_r, T_c
+
+
+def tile_stats_elems(shape: Shape) -> int:
+    return int(load().bl_tile_stats_elems(ctypes.byref(shape)))
+
+
+def bwd_workspace_bytes(shape: Shape) -> int:
+    return int(load().bl_bwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def attn_fwd(shape, q, k, v, scale, o, lse, tile_stats=None):
+    B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
+    _need(q, torch.bfloat16, (B, n, H, d), "q")
+    _need(k, torch.bfloat16, (B, n, Hk, d), "k")
+    _need(v, torch.bfloat16, (B, n, Hk, d), "v")
+    _need(o, torch.bfloat16, (B, n, H, d), "o")
+    _need(lse, torch.float32, (B, H, n), "lse")
+    if tile_stats is not None:
+        T_r, T_c = tiles(shape)
+        _need(tile_stats, torch.float32, (B, H, T_c, T_r * shape.block_q), "tile_stats")
+    code = load().bl_attn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), float(scale),
+                              _ptr(o), _ptr(lse), _ptr(tile_stats), _stream(q.device))
+    _check("bl_attn_fwd", code)
+
+
+def alloc_lists(shape: Shape, device) -> dict:
+    T_r, T_c = tiles(shape)
+    B, H = shape.B, shape.H
+    return {
+        "mask": torch.empty((B, H, T_r, T_c), dtype=torch.uint8, device=device),
+        "kv_idx": torch.empty((B, H, T_r, T_c), dtype=torch.int32, device=device),
+        "kv_cnt": torch.empty((B, H, T_r), dtype=torch.int32, device=device),
+        "q_idx": torch.empty((B, H, T_c, T_r), dtype=torch.int32, device=device),
+        "q_cnt": torch.empty((B, H, T_c), dtype=torch.int32, device=device),
+        "nan_count": torch.zeros((1,), dtype=torch.int32, device=device),
+    }
+
+
+def _lists_struct(lists):
+    return Lists(_ptr(lists["mask"]), _ptr(lists["kv_idx"]), _ptr(lists["kv_cnt"]),
+                 _ptr(lists["q_idx"]), _ptr(lists["q_cnt"]), _ptr(lists.get("nan_count")))
+
+
+def mask_from_stats(shape, tile_stats, lse, negl_prob, lists):
+    B, H, n = shape.B, shape.H, shape.n
+    T_r, T_c = tiles(shape)
+    _need(tile_stats, torch.float32, (B, H, T_c, T_r * shape.block_q), "tile_stats")
+    _need(lse, torch.float32, (B, H, n), "lse")
+    _need(lists["mask"], torch.uint8, (B, H, T_r, T_c), "mask")
+    _need(lists["kv_idx"], torch.int32, (B, H, T_r, T_c), "kv_idx")
+    _need(lists["kv_cnt"], torch.int32, (B, H, T_r), "kv_cnt")
+    _need(lists["q_idx"], torch.int32, (B, H, T_c, T_r), "q_idx")
+    _need(lists["q_cnt"], torch.int32, (B, H, T_c), "q_cnt")
+    ls = _lists_struct(lists)
+    code = load().bl_mask_from_stats(ctypes.byref(shape), _ptr(tile_stats), _ptr(lse),
+                                     float(negl_prob), ctypes.byref(ls), _stream(lse.device))
+    _check("bl_mask_from_stats", code)
+
+
+def attn_bwd(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, workspace):
+    B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
+    for t, nm, sh in ((q, "q", (B, n, H, d)), (k, "k", (B, n, Hk, d)), (v, "v", (B, n, Hk, d)),
+                      (o, "o", (B, n, H, d)), (g_o, "g_o", (B, n, H, d)),
+                      (g_q, "g_q", (B, n, H, d)), (g_k, "g_k", (B, n, Hk, d)),
+                      (g_v, "g_v", (B, n, Hk, d))):
+        _need(t, torch.bfloat16, sh, nm)
+    _need(lse, torch.float32, (B, H, n), "lse")
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    ls = None
+    if lists is not None:
+        T_r, T_c = tiles(shape)
+        _need(lists["q_idx"], torch.int32, (B, H, T_c, T_r), "q_idx")
+        _need(lists["q_cnt"], torch.int32, (B, H, T_c), "q_cnt")
+        ls = _lists_struct(lists)
+    code = load().bl_attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(g_o),
+                              _ptr(lse), float(scale),
+                              ctypes.byref(ls) if ls is not None else None,
+                              _ptr(g_q), _ptr(g_k), _ptr(g_v), _ptr(workspace),
+                              workspace.numel(), _stream(q.device))
+    _check("bl_attn_bwd", code)
+
+
+def bwd_check_status(shape, workspace) -> int:
+    return int(load().bl_bwd_check_status(ctypes.byref(shape), _ptr(workspace),
+                                          _stream(workspace.device)))

@@ -1,0 +1,95 @@
+"""User-facing BackLite attention on the bl_attn C ABI.
+
+``BLAttention(negl_prob)`` mirrors the module the "BackLite" README describes
+(Usage, Forward signature): it is called as
+``attn(query, key, value, scale=None, return_softmax_lse=False, tile_stats=None)``
+on (batch, seq_len, heads, head_dim) bf16 tensors, with key/value carrying
+``heads_k`` heads.  With negl_prob > 0 the forward records tile statistics
+(allocating the buffer unless one is passed, README, Note) and the backward
+builds the block-sparse mask from them before running the sparse backward
+(How It Works, Phase 2).  negl_prob = 0 records nothing and runs the dense
+backward (Key properties).  ``BL_VERBOSE=1`` prints mask density per head
+after each mask pass (README, Debugging, names the same kind of switch).
+
+PyTorch only allocates memory and supplies the stream; all arithmetic runs in
+libbl_attn.so.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import torch
+
+from . import _lib
+
+
+def default_tiles(n: int, d: int):
+    """Tile sizes used when the caller does not choose: 128 x 128."""
+    return 128, 128
+
+
+class _BLAttnFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, scale, negl_prob, block_q, block_k, tile_stats):
+        B, n, H, d = q.shape
+        Hk = k.shape[2]
+        shape = _lib.make_shape(B, n, H, Hk, d, block_q, block_k)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
+        stats = None
+        if negl_prob > 0:
+            T_r, T_c = _lib.tiles(shape)
+            want = (B, H, T_c, T_r * block_q)
+            stats = tile_stats if tile_stats is not None else torch.empty(
+                want, dtype=torch.float32, device=q.device)
+        _lib.attn_fwd(shape, q, k, v, scale, o, lse, stats)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.stats = stats
+        ctx.cfg = (shape, scale, negl_prob)
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, g_o, _g_lse):
+        q, k, v, o, lse = ctx.saved_tensors
+        shape, scale, negl_prob = ctx.cfg
+        g_o = g_o.contiguous()
+        lists = None
+        if ctx.stats is not None:
+            lists = _lib.alloc_lists(shape, q.device)
+            _lib.mask_from_stats(shape, ctx.stats, lse, negl_prob, lists)
+            if os.environ.get("BL_VERBOSE") == "1":
+                m = lists["mask"].float()
+                dens = m.mean(dim=(2, 3)).cpu()
+                print(f"[bl_attn] mask density per (batch, head): {dens.tolist()} "
+                      f"backward skip fraction {1.0 - float(m.mean()):.4f}")
+        g_q = torch.empty_like(q)
+        g_k = torch.empty_like(k)
+        g_v = torch.empty_like(v)
+        ws = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=q.device)
+        _lib.attn_bwd(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, ws)
+        return g_q, g_k, g_v, None, None, None, None, None
+
+
+class BLAttention(torch.nn.Module):
+    """Attention whose backward skips the lightest tiles (negl_prob of the mass)."""
+
+    def __init__(self, negl_prob: float = 0.05, block_q: int | None = None,
+                 block_k: int | None = None):
+        super().__init__()
+        if not (0.0 <= negl_prob < 1.0):
+            raise ValueError("negl_prob must lie in [0, 1)")
+        self.negl_prob = float(negl_prob)
+        self.block_q, self.block_k = block_q, block_k
+
+    def forward(self, query, key, value, scale=None, return_softmax_lse=False, tile_stats=None):
+        d = query.shape[-1]
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        bq, bk = default_tiles(query.shape[1], d)
+        bq = self.block_q or bq
+        bk = self.block_k or bk
+        q, k, v = (t.contiguous() for t in (query, key, value))
+        o, lse = _BLAttnFn.apply(q, k, v, float(scale), self.negl_prob, bq, bk, tile_stats)
+        return (o, lse) if return_softmax_lse else o

@@ -1,0 +1,140 @@
+// C ABI of libbl_attn.so: argument validation, workspace layout, launches.
+// The operations and layouts are documented in include/bl_attn.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/bl_attn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bl_status check_shape(const bl_shape* s, bl::Shape* out) {
+  if (!s) return BL_ERR_INVALID_ARG;
+  if (s->B < 1 || s->n < 1 || s->H < 1 || s->Hk < 1 || s->H % s->Hk != 0)
+    return BL_ERR_INVALID_ARG;
+  if (s->B > 65535 || s->H > 65535) return BL_ERR_UNSUPPORTED;
+  if (s->d != 64 && s->d != 128) return BL_ERR_UNSUPPORTED;
+  if ((s->block_q != 64 && s->block_q != 128) || (s->block_k != 64 && s->block_k != 128))
+    return BL_ERR_UNSUPPORTED;
+  bl::Shape sh;
+  sh.B = s->B; sh.n = s->n; sh.H = s->H; sh.Hk = s->Hk; sh.d = s->d;
+  sh.block_q = s->block_q; sh.block_k = s->block_k;
+  sh.T_r = (s->n + s->block_q - 1) / s->block_q;
+  sh.T_c = (s->n + s->block_k - 1) / s->block_k;
+  sh.n_pad = (int64_t)sh.T_r * s->block_q;
+  *out = sh;
+  return BL_OK;
+}
+
+size_t ws_D_bytes(const bl::Shape& sh) {
+  size_t b = (size_t)sh.B * sh.H * sh.n * sizeof(float);
+  return (b + 255) & ~(size_t)255;
+}
+size_t ws_dq_bytes(const bl::Shape& sh) {
+  return (size_t)sh.B * sh.n * sh.H * sh.d * sizeof(float);
+}
+
+bl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t bl_tile_stats_elems(const bl_shape* shape) {
+  bl::Shape sh;
+  if (check_shape(shape, &sh) != BL_OK) return 0;
+  return (size_t)sh.B * sh.H * sh.T_c * (size_t)sh.n_pad;
+}
+
+size_t bl_bwd_workspace_bytes(const bl_shape* shape) {
+  bl::Shape sh;
+  if (check_shape(shape, &sh) != BL_OK) return 0;
+  return ws_D_bytes(sh) + ws_dq_bytes(sh) + 256;
+}
+
+bl_status bl_attn_fwd(const bl_shape* shape, const void* q, const void* k, const void* v,
+                      float scale, void* o, float* lse, float* tile_stats, void* stream) {
+  bl::Shape sh;
+  bl_status s = check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  if (!q || !k || !v || !o || !lse) return BL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (tile_stats && !aligned16(tile_stats)))
+    return BL_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
+  return cuda_status(bl::launch_fwd(sh, q, k, v, o, lse, tile_stats, scale, (cudaStream_t)stream));
+}
+
+bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats, const float* lse,
+                             double negl_prob, const bl_lists* lists, void* stream) {
+  bl::Shape sh;
+  bl_status s = check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  if (!tile_stats || !lse || !lists) return BL_ERR_INVALID_ARG;
+  if (!lists->mask || !lists->kv_idx || !lists->kv_cnt || !lists->q_idx || !lists->q_cnt)
+    return BL_ERR_INVALID_ARG;
+  if (!aligned16(tile_stats) || !aligned16(lse)) return BL_ERR_INVALID_ARG;
+  if (!(negl_prob >= 0.0) || !(negl_prob < 1.0)) return BL_ERR_INVALID_ARG;
+  if (sh.T_c > 2048) return BL_ERR_UNSUPPORTED;
+  // T = ceil(negl_prob * 2^40): the product is exact in fp64.
+  unsigned long long T = (unsigned long long)ceil(negl_prob * 1099511627776.0);
+  return cuda_status(bl::launch_mask(sh, tile_stats, lse, T, lists->mask, lists->kv_idx,
+                                     lists->kv_cnt, lists->q_idx, lists->q_cnt,
+                                     lists->nan_count, (cudaStream_t)stream));
+}
+
+bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k, const void* v,
+                      const void* o, const void* g_o, const float* lse, float scale,
+                      const bl_lists* lists, void* g_q, void* g_k, void* g_v, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  bl::Shape sh;
+  bl_status s = check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  const void* ptrs[] = {q, k, v, o, g_o, lse, g_q, g_k, g_v};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return BL_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
+  if (lists && (!lists->q_idx || !lists->q_cnt)) return BL_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return BL_ERR_WORKSPACE;
+  if (workspace_bytes < bl_bwd_workspace_bytes(shape)) return BL_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* ws_D = reinterpret_cast<float*>(ws);
+  float* ws_dq = reinterpret_cast<float*>(ws + ws_D_bytes(sh));
+  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + ws_D_bytes(sh) + ws_dq_bytes(sh));
+  return cuda_status(bl::launch_bwd(sh, q, k, v, o, g_o, lse, scale,
+                                    lists ? lists->q_idx : nullptr, lists ? lists->q_cnt : nullptr,
+                                    g_q, g_k, g_v, ws_D, ws_dq, ws_status, (cudaStream_t)stream));
+}
+
+bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace, void* stream) {
+  bl::Shape sh;
+  bl_status s = check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  if (!workspace) return BL_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const int32_t* st = reinterpret_cast<const int32_t*>(ws + ws_D_bytes(sh) + ws_dq_bytes(sh));
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, st, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return BL_ERR_CUDA;
+  return host ? BL_ERR_CORRUPT_LISTS : BL_OK;
+}
+
+const char* bl_status_string(bl_status status) {
+  switch (status) {
+    case BL_OK: return "ok";
+    case BL_ERR_INVALID_ARG: return "invalid argument";
+    case BL_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BL_ERR_CUDA: return "CUDA error";
+    case BL_ERR_WORKSPACE: return "workspace missing or too small";
+    case BL_ERR_CORRUPT_LISTS: return "tile list entry out of range";
+    case BL_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

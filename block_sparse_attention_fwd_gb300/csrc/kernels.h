@@ -1,0 +1,30 @@
+// Host-side launchers of the bl_attn kernels (internal to libbl_attn.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bl {
+
+struct Shape;
+
+// Forward + optional tile statistics (stats == nullptr skips them).
+cudaError_t launch_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o,
+                       float* lse, float* stats, float scale, cudaStream_t st);
+
+// Tile selection: per-query-tile mask row, kv list and count, then the
+// transposed per-key-tile q list and count.
+cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
+                        unsigned long long threshold, uint8_t* mask, int32_t* kv_idx,
+                        int32_t* kv_cnt, int32_t* q_idx, int32_t* q_cnt, int32_t* nan_count,
+                        cudaStream_t st);
+
+// Backward.  q_idx/q_cnt == nullptr runs every tile.  ws_D [B,H,n] fp32,
+// ws_dq [B,n,H,d] fp32, ws_status one int32.
+cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void* v,
+                       const void* o, const void* g_o, const float* lse, float scale,
+                       const int32_t* q_idx, const int32_t* q_cnt, void* g_q, void* g_k,
+                       void* g_v, float* ws_D, float* ws_dq, int32_t* ws_status,
+                       cudaStream_t st);
+
+}  // namespace bl

@@ -1,0 +1,275 @@
+// mask_from_stats: tile statistics -> block-sparse mask and tile lists.
+//
+// "BackLite" README, How It Works, Phase 2: per tile pair the weight is
+// p_tile = exp(LSE_tile - LSE_row), and the smallest-weight tiles whose
+// cumulative weight stays below negl_prob are skipped.  Key properties:
+// "cumulative weight < negl_prob" (strict) and negl_prob = 0 keeps every
+// tile.  "Introducing BackLite", Using Sparsity: a skipped tile costs no
+// loads and no FLOPs in the backward.
+//
+// The rule as implemented (the pages leave the reduction, tie-break and
+// arithmetic open):
+//   d_ij = max over rows r < n of query tile i of fp32(stats[j][r] - lse[r]),
+//          NaN if any term is NaN, then clamped to <= 0 with -0 -> +0;
+//   E_ij = ceil(detexp(d_ij) * 2^40) as a 64-bit integer;
+//   per query tile, order the non-NaN key tiles by (d asc, j asc) and skip
+//   the longest prefix whose integer running sum is < ceil(negl_prob*2^40).
+// detexp is a fixed sequence of round-to-nearest fp32 operations (no FMA):
+//   t = d*log2(e); t < -48 -> E = 1; k = rint(t); f = t - k;
+//   p = Horner over the degree-7 Taylor polynomial of 2^f = exp(f ln 2);
+//   e = p * 2^k.  Integer sums make the result independent of the order in
+//   which a parallel scan adds them.
+//
+// Kernel 1: one CTA per (query tile, head, batch).  Warps stream the
+// statistics of the tile's rows (coalesced 256/512-byte rows per key tile),
+// reduce d_ij, then the CTA sorts (key, E) pairs with a bitonic network in
+// shared memory, scans E, and writes the mask row plus the compacted kv list.
+// Kernel 2: one warp per (key tile, head, batch) compacts the mask column
+// into the ascending q list with ballots.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bl {
+
+namespace {
+
+constexpr int kMaskThreads = 256;
+constexpr int kMaxTc = 2048;
+
+// fp32 nearest to log2(e) and to (ln 2)^m / m!, m = 0..7 (Taylor series of 2^f).
+__device__ __forceinline__ uint64_t detexp_fixed40(float d) {
+  if (isinf(d)) return 0ull;  // d == -inf: the tile has no weight
+  const float log2e = __uint_as_float(0x3fb8aa3bu);
+  const float c0 = __uint_as_float(0x3f800000u), c1 = __uint_as_float(0x3f317218u),
+              c2 = __uint_as_float(0x3e75fdf0u), c3 = __uint_as_float(0x3d635847u),
+              c4 = __uint_as_float(0x3c1d955bu), c5 = __uint_as_float(0x3aaec3ffu),
+              c6 = __uint_as_float(0x39218489u), c7 = __uint_as_float(0x377fe5feu);
+  float t = __fmul_rn(d, log2e);
+  if (t < -48.f) return 1ull;
+  float kf = rintf(t);
+  float f = __fsub_rn(t, kf);
+  float p = c7;
+  p = __fadd_rn(__fmul_rn(p, f), c6);
+  p = __fadd_rn(__fmul_rn(p, f), c5);
+  p = __fadd_rn(__fmul_rn(p, f), c4);
+  p = __fadd_rn(__fmul_rn(p, f), c3);
+  p = __fadd_rn(__fmul_rn(p, f), c2);
+  p = __fadd_rn(__fmul_rn(p, f), c1);
+  p = __fadd_rn(__fmul_rn(p, f), c0);
+  int ki = (int)kf;                                   // -48 <= ki <= 0
+  float e = __fmul_rn(p, __uint_as_float((uint32_t)(ki + 127) << 23));
+  float s = __fmul_rn(e, 1099511627776.0f);           // * 2^40, exact
+  return (uint64_t)__float2ull_rn(ceilf(s));
+}
+
+__device__ __forceinline__ uint32_t order_key(float d) {
+  uint32_t u = __float_as_uint(d);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int RPL>  // rows per lane: block_q / 32
+__global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
+    const float* __restrict__ stats, const float* __restrict__ lse, Shape sh,
+    unsigned long long T, uint8_t* __restrict__ mask, int32_t* __restrict__ kv_idx,
+    int32_t* __restrict__ kv_cnt, int32_t* __restrict__ nan_count) {
+  __shared__ float s_d[kMaxTc];
+  __shared__ unsigned long long s_key[kMaxTc];
+  __shared__ unsigned long long s_E[kMaxTc];
+  __shared__ unsigned long long s_wsum[kMaskThreads / 32];
+  __shared__ int s_wcnt[kMaskThreads / 32];
+  __shared__ uint8_t s_act[kMaxTc];
+
+  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Tc = sh.T_c;
+  const int64_t bh = (int64_t)b * sh.H + h;
+  const int r0 = i * sh.block_q + lane * RPL;
+
+  float lrow[RPL];
+  bool valid[RPL];
+#pragma unroll
+  for (int e = 0; e < RPL; ++e) {
+    valid[e] = (r0 + e) < sh.n;
+    lrow[e] = valid[e] ? lse[bh * sh.n + r0 + e] : 0.f;
+  }
+  const float* st = stats + bh * sh.T_c * sh.n_pad + r0;
+  for (int j = warp; j < Tc; j += kMaskThreads / 32) {
+    float vals[RPL];
+    if constexpr (RPL == 4) {
+      float4 x = *reinterpret_cast<const float4*>(st + (int64_t)j * sh.n_pad);
+      vals[0] = x.x; vals[1] = x.y; vals[2] = x.z; vals[3] = x.w;
+    } else {
+      float2 x = *reinterpret_cast<const float2*>(st + (int64_t)j * sh.n_pad);
+      vals[0] = x.x; vals[1] = x.y;
+    }
+    float mx = -INFINITY;
+    bool nan = false;
+#pragma unroll
+    for (int e = 0; e < RPL; ++e) {
+      if (!valid[e]) continue;
+      float dv = __fsub_rn(vals[e], lrow[e]);
+      if (isnan(dv)) nan = true;
+      else mx = fmaxf(mx, dv);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    bool any_nan = __any_sync(0xffffffffu, nan);
+    if (lane == 0) {
+      float dv = any_nan ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
+      if (dv == 0.f) dv = 0.f;  // -0 -> +0
+      s_d[j] = dv;
+    }
+  }
+  __syncthreads();
+
+  int P2 = 1;
+  while (P2 < Tc) P2 <<= 1;
+  int local_nan = 0;
+  for (int m = tid; m < P2; m += kMaskThreads) {
+    unsigned long long key = ~0ull, E = 0ull;
+    if (m < Tc) {
+      float dv = s_d[m];
+      if (isnan(dv)) {
+        key = (0xffffffffull << 32) | (unsigned)m;
+        ++local_nan;
+      } else {
+        key = ((unsigned long long)order_key(dv) << 32) | (unsigned)m;
+        E = detexp_fixed40(dv);
+      }
+      s_act[m] = 1;
+    }
+    s_key[m] = key;
+    s_E[m] = E;
+  }
+  if (nan_count) {
+    local_nan = __reduce_add_sync(0xffffffffu, local_nan);
+    if (lane == 0 && local_nan) atomicAdd(nan_count, local_nan);
+  }
+  __syncthreads();
+
+  // bitonic sort of (key, E) ascending by key
+  for (int kk = 2; kk <= P2; kk <<= 1) {
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      for (int tt = tid; tt < (P2 >> 1); tt += kMaskThreads) {
+        int a = (tt / jj) * 2 * jj + (tt % jj);
+        int c = a + jj;
+        bool up = (a & kk) == 0;
+        unsigned long long ka = s_key[a], kc = s_key[c];
+        if ((ka > kc) == up) {
+          s_key[a] = kc;
+          s_key[c] = ka;
+          unsigned long long ea = s_E[a];
+          s_E[a] = s_E[c];
+          s_E[c] = ea;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // inclusive scan of E in sorted order; count positions with prefix < T
+  // among the non-NaN entries (NaN and padding keys sort last).
+  constexpr int PER = kMaxTc / kMaskThreads;  // <= 8 elements per thread
+  int per = (P2 + kMaskThreads - 1) / kMaskThreads;
+  int base = tid * per;
+  unsigned long long run = 0ull;
+  for (int e = 0; e < per && e < PER; ++e) {
+    int m = base + e;
+    if (m < P2) run += s_E[m];
+  }
+  // exclusive scan of per-thread totals
+  unsigned long long incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  unsigned long long woff = 0ull;
+  for (int w = 0; w < warp; ++w) woff += s_wsum[w];
+  unsigned long long pre = woff + incl - run;
+  int nskip = 0;
+  for (int e = 0; e < per && e < PER; ++e) {
+    int m = base + e;
+    if (m >= P2) break;
+    unsigned long long key = s_key[m];
+    pre += s_E[m];
+    if ((key >> 32) != 0xffffffffull && pre < T) ++nskip;
+  }
+  __syncthreads();
+  // the skipped entries form a prefix of the sorted order: mark them
+  for (int e = 0; e < per && e < PER; ++e) {
+    int m = base + e;
+    if (m < P2 && e < nskip) s_act[(int)(s_key[m] & 0xffffffffull)] = 0;
+  }
+  __syncthreads();
+
+  // write the mask row and the ascending kv list
+  uint8_t* mrow = mask + (bh * sh.T_r + i) * (int64_t)Tc;
+  int32_t* krow = kv_idx + (bh * sh.T_r + i) * (int64_t)Tc;
+  int cnt_run = 0;
+  for (int j0 = 0; j0 < Tc; j0 += kMaskThreads) {
+    int j = j0 + tid;
+    int f = (j < Tc) ? s_act[j] : 0;
+    if (j < Tc) mrow[j] = (uint8_t)f;
+    unsigned bal = __ballot_sync(0xffffffffu, f);
+    int wpos = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) s_wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int off = cnt_run;
+    for (int w = 0; w < warp; ++w) off += s_wcnt[w];
+    if (f) krow[off + wpos] = j;
+    int tot = 0;
+    for (int w = 0; w < kMaskThreads / 32; ++w) tot += s_wcnt[w];
+    __syncthreads();
+    cnt_run += tot;
+  }
+  for (int j = cnt_run + tid; j < Tc; j += kMaskThreads) krow[j] = -1;
+  if (tid == 0) kv_cnt[bh * sh.T_r + i] = cnt_run;
+}
+
+__global__ void __launch_bounds__(256) q_lists_kernel(const uint8_t* __restrict__ mask, Shape sh,
+                                                      int32_t* __restrict__ q_idx,
+                                                      int32_t* __restrict__ q_cnt) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 8 + warp;
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (j >= sh.T_c) return;
+  const int64_t bh = (int64_t)b * sh.H + h;
+  const uint8_t* mcol = mask + bh * sh.T_r * (int64_t)sh.T_c + j;
+  int32_t* qrow = q_idx + (bh * sh.T_c + j) * (int64_t)sh.T_r;
+  int cnt = 0;
+  for (int i0 = 0; i0 < sh.T_r; i0 += 32) {
+    int i = i0 + lane;
+    int f = (i < sh.T_r) ? mcol[(int64_t)i * sh.T_c] : 0;
+    unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (f) qrow[cnt + __popc(bal & ((1u << lane) - 1u))] = i;
+    cnt += __popc(bal);
+  }
+  for (int i = cnt + lane; i < sh.T_r; i += 32) qrow[i] = -1;
+  if (lane == 0) q_cnt[bh * sh.T_c + j] = cnt;
+}
+
+}  // namespace
+
+cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
+                        unsigned long long threshold, uint8_t* mask, int32_t* kv_idx,
+                        int32_t* kv_cnt, int32_t* q_idx, int32_t* q_cnt, int32_t* nan_count,
+                        cudaStream_t st) {
+  if (sh.T_c > kMaxTc) return cudaErrorInvalidValue;
+  dim3 g1(sh.T_r, sh.H, sh.B);
+  if (sh.block_q == 128)
+    mask_rows_kernel<4><<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx,
+                                                     kv_cnt, nan_count);
+  else
+    mask_rows_kernel<2><<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx,
+                                                     kv_cnt, nan_count);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2((sh.T_c + 7) / 8, sh.H, sh.B);
+  q_lists_kernel<<<g2, 256, 0, st>>>(mask, sh, q_idx, q_cnt);
+  return cudaGetLastError();
+}
+
+}  // namespace bl

@@ -1,0 +1,156 @@
+/*
+ * bl_attn.h -- C ABI of libbl_attn.so: BackLite-style attention on GB300.
+ *
+ * Three calls make up the hot path, in this order:
+ *
+ *   bl_attn_fwd         exact attention forward that also records, for every
+ *                       (query row, key tile), the log-sum-exp of that row's
+ *                       scores over the tile ("BackLite" README, How It Works,
+ *                       Phase 1; "Introducing BackLite", Using Sparsity).
+ *   bl_mask_from_stats  turns those statistics into a block-sparse mask and
+ *                       compacted tile lists (README, How It Works, Phase 2).
+ *   bl_attn_bwd         attention backward that reads and computes nothing
+ *                       for masked tiles ("Introducing BackLite",
+ *                       Backpropagation for attention, and Using Sparsity).
+ *
+ * Tensors
+ *   q, o, g_o, g_q : [B, n, H,  d] bf16, contiguous (batch, seq, head, dim)
+ *   k, v, g_k, g_v : [B, n, Hk, d] bf16, contiguous; query head h reads kv
+ *                    head h / (H / Hk) (grouped-query attention, README,
+ *                    Forward signature: key/value carry heads_k heads).
+ *   lse            : [B, H, n] fp32, natural log: LSE_r = log sum_c exp(s q_r.k_c)
+ *   tile_stats     : [B, H, T_c, T_r*block_q] fp32, key-tile major:
+ *                    tile_stats[b,h,j,r] = log sum_{c in key tile j} exp(s q_r.k_c);
+ *                    -inf where the tile's terms underflow and for rows r >= n.
+ *   T_r = ceil(n / block_q), T_c = ceil(n / block_k).
+ *
+ * Every pointer is device memory owned by the caller; the library allocates
+ * nothing and frees nothing.  Calls are asynchronous on the given stream
+ * (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ * Arguments are validated on the host before any launch: a failing check
+ * launches nothing and returns an error code.  Device pointers must be
+ * 16-byte aligned.
+ */
+#ifndef BL_ATTN_H
+#define BL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BL_OK = 0,
+  BL_ERR_INVALID_ARG = 1,    /* bad shape, pointer, alignment or parameter   */
+  BL_ERR_UNSUPPORTED = 2,    /* valid but not built (e.g. head_dim 96)       */
+  BL_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed         */
+  BL_ERR_WORKSPACE = 4,      /* workspace missing or too small               */
+  BL_ERR_CORRUPT_LISTS = 5,  /* a tile list held an out-of-range entry       */
+  BL_ERR_TIMEOUT = 6         /* a bounded device-side wait ran out           */
+} bl_status;
+
+/* Problem shape.  d in {64, 128}; block_q, block_k in {64, 128}; H % Hk == 0;
+ * n >= 1.  One shape describes the forward, the mask and the backward: the
+ * statistics, the mask and the backward all use the same block_q x block_k
+ * tiles. */
+typedef struct {
+  int B, n, H, Hk, d;
+  int block_q, block_k;
+} bl_shape;
+
+/* Block-sparse tile lists of one backward, all device memory.
+ *   mask   [B,H,T_r,T_c] uint8   1 = compute tile (i, j), 0 = skip
+ *   kv_idx [B,H,T_r,T_c] int32   per query tile: active key tiles, ascending,
+ *                                then -1 up to T_c
+ *   kv_cnt [B,H,T_r]     int32   number of active key tiles per query tile
+ *   q_idx  [B,H,T_c,T_r] int32   per key tile: active query tiles, ascending,
+ *                                then -1 up to T_r
+ *   q_cnt  [B,H,T_c]     int32   number of active query tiles per key tile
+ *   nan_count            int32*  optional (may be NULL): the mask pass adds
+ *                                the number of NaN tile weights it met (such
+ *                                tiles are kept).  The caller zeroes it.
+ * The mask is per query head: the heads of one GQA group each have their own
+ * lists ("BackLite" README, Key properties: sparsity per sample, per head). */
+typedef struct {
+  uint8_t* mask;
+  int32_t* kv_idx;
+  int32_t* kv_cnt;
+  int32_t* q_idx;
+  int32_t* q_cnt;
+  int32_t* nan_count;
+} bl_lists;
+
+/* Number of fp32 elements of tile_stats: B*H*T_c*T_r*block_q. */
+size_t bl_tile_stats_elems(const bl_shape* shape);
+
+/* Bytes of device workspace bl_attn_bwd needs (16-byte aligned base):
+ * D = rowsum(G_O * O) [B,H,n] fp32, the fp32 dQ accumulator [B,n,H,d] and a
+ * device status word. */
+size_t bl_bwd_workspace_bytes(const bl_shape* shape);
+
+/* Exact attention forward ("Introducing BackLite", Backpropagation for
+ * attention: S = s Q K^T, P = softmax_row(S), O = P V; the forward is not
+ * approximated, Using Sparsity).
+ *   scale       softmax scale s (finite, > 0); 1/sqrt(d) is the usual value.
+ *   o, lse      outputs (layouts above).
+ *   tile_stats  output, or NULL to skip recording the statistics (the
+ *               negl_prob = 0 path: README, Key properties, zero forward
+ *               overhead when nothing will be skipped).
+ * Errors: BL_ERR_INVALID_ARG (shape, pointers, alignment, scale),
+ *         BL_ERR_UNSUPPORTED (d or tile size), BL_ERR_CUDA (launch). */
+bl_status bl_attn_fwd(const bl_shape* shape, const void* q, const void* k,
+                      const void* v, float scale, void* o, float* lse,
+                      float* tile_stats, void* stream);
+
+/* Tile selection (README, How It Works, Phase 2; Key properties).  For
+ * every (b, h, query tile i) and key tile j:
+ *   d_ij = max over rows r < n of tile i of fp32(tile_stats[b,h,j,r] - lse[b,h,r]),
+ *          clamped to <= 0, so w_ij = exp(d_ij) bounds the weight any row of
+ *          the tile puts on key tile j;
+ *   E_ij = ceil(detexp(d_ij) * 2^40), a 40-bit fixed-point weight (detexp is
+ *          an exp evaluated by a fixed sequence of round-to-nearest fp32
+ *          operations, so every implementation gets the same integers);
+ *   the key tiles are ordered by (d ascending, j ascending) and the longest
+ *   prefix whose integer running sum stays below ceil(negl_prob * 2^40) is
+ *   skipped.  negl_prob = 0 skips nothing.
+ * Writes every field of *lists (layouts above).
+ * Errors: BL_ERR_INVALID_ARG (negl_prob outside [0, 1), null pointers),
+ *         BL_ERR_UNSUPPORTED (T_c > 2048), BL_ERR_CUDA. */
+bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats,
+                             const float* lse, double negl_prob,
+                             const bl_lists* lists, void* stream);
+
+/* Masked attention backward ("Introducing BackLite", Backpropagation for
+ * attention and Using Sparsity), with M the element mask expanded from
+ * lists->mask and P recomputed from the full-row lse:
+ *   D = rowsum(G_O * O), P^ = P * M, G_V = P^T G_O, G_P = G_O V^T,
+ *   G_S = P^ * (G_P - D), G_Q = s G_S K, G_K = s G_S^T Q
+ * (kv-head gradients sum over the query heads of their group).  Tiles not
+ * in the lists are neither loaded nor computed.  lists == NULL runs the
+ * dense backward (every tile).  Only q_idx/q_cnt of the lists are read.
+ *   workspace  device buffer of at least bl_bwd_workspace_bytes(shape).
+ * Errors: BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED, BL_ERR_WORKSPACE,
+ *         BL_ERR_CUDA.  A list entry outside [0, T_r) (or a count outside
+ *         [0, T_r]) is skipped on the device and recorded in the status word;
+ *         bl_bwd_check_status reports it as BL_ERR_CORRUPT_LISTS. */
+bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k,
+                      const void* v, const void* o, const void* g_o,
+                      const float* lse, float scale, const bl_lists* lists,
+                      void* g_q, void* g_k, void* g_v, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Synchronises the stream and reads the status word a previous bl_attn_bwd
+ * left in this workspace: BL_OK, or BL_ERR_CORRUPT_LISTS. */
+bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace,
+                              void* stream);
+
+/* Static description of a status code. */
+const char* bl_status_string(bl_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BL_ATTN_H */

@@ -31,12 +31,14 @@ Readings where the pages are silent: the LSE is the natural-log
 log-sum-exp of the scaled scores s*q.k (the README's p_tile formula uses exp);
 a tile LSE is taken per query row and key tile; a tile whose exponentials all
 underflow has LSE -inf; rows r >= n of the last query tile do not exist and
-their stats entries are -inf; D uses the exact forward output and the full
-row LSE (no renormalisation over the kept tiles).
+their stats entries are -inf; D is formed from the forward output as it is
+stored (bf16, see ``as_stored_output``) and P from the full-row LSE (no
+renormalisation over the kept tiles).
 """
 from __future__ import annotations
 
 import numpy as np
+import torch
 
 ROW_GROUP = 2048
 
@@ -133,6 +135,15 @@ def forward(q, k, v, scale, block_q=None, block_k=None):
     return O, LSE, stats
 
 
+def as_stored_output(O) -> np.ndarray:
+    """The forward output as the method hands it on: the output tensor has the
+    inputs' dtype (bf16), so O is the exact result rounded to nearest-even
+    bf16.  D = rowsum(G_O (.) O) in the backward is formed from this stored O,
+    the same tensor any caller passes back in."""
+    t = torch.from_numpy(np.ascontiguousarray(O, dtype=np.float64)).to(torch.bfloat16)
+    return t.double().numpy()
+
+
 def element_mask(tile_mask: np.ndarray, block_q: int, block_k: int,
                  rows: np.ndarray, cols: np.ndarray) -> np.ndarray:
     """Expand a [T_r, T_c] tile mask to the element mask M[rows][:, cols]."""
@@ -183,7 +194,8 @@ def backward(q, k, v, o, g_o, lse, scale, tile_masks=None, block_q=None,
     """Masked attention backward over BSHD tensors (full, every row/column).
 
     ``tile_masks``: [B, H, T_r, T_c] (nonzero = compute), or None for dense.
-    ``o`` and ``lse`` are the oracle's own forward results.  Returns fp64
+    ``o`` is the forward output as stored (``as_stored_output`` of the oracle's
+    own O) and ``lse`` the oracle's own LSE.  Returns fp64
     G_Q [B,n,H,d], G_K and G_V [B,n,Hk,d]; the gradient of a kv head sums the
     contributions of every query head in its group.
     """

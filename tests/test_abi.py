@@ -1,0 +1,112 @@
+"""The C ABI library builds, loads, exports every declared symbol and rejects
+bad arguments on the host before any launch (CPU only: no compute call
+reaches a GPU here)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bl_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_attention_fwd_gb300 import _lib, build
+    if not os.path.exists(_lib.LIB_PATH) or not build.up_to_date():
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("nvcc not available to build libbl_attn.so")
+        build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bl_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    from block_sparse_attention_fwd_gb300 import _lib
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _shape(**kw):
+    from block_sparse_attention_fwd_gb300 import _lib
+    a = dict(B=1, n=256, H=2, Hk=1, d=64, block_q=64, block_k=64)
+    a.update(kw)
+    return _lib.make_shape(**a)
+
+
+def test_size_queries(lib):
+    from block_sparse_attention_fwd_gb300 import _lib
+    s = _shape(n=1000, block_q=128, block_k=64)
+    assert _lib.tile_stats_elems(s) == 1 * 2 * 16 * (8 * 128)
+    ws = _lib.bwd_workspace_bytes(s)
+    assert ws >= 2 * 1000 * 4 + 1000 * 2 * 64 * 4 + 4
+    assert _lib.tile_stats_elems(_shape(d=96)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), 2), (dict(H=3, Hk=2), 1), (dict(n=0), 1), (dict(block_k=32), 2),
+    (dict(B=0), 1)])
+def test_fwd_rejects_bad_shapes_without_launching(lib, kw, code):
+    s = _shape(**kw)
+    fake = ctypes.c_void_p(0x10000)
+    r = lib.bl_attn_fwd(ctypes.byref(s), fake, fake, fake, 0.125, fake, fake, None, None)
+    assert r == code
+
+
+def test_fwd_rejects_bad_pointers_and_scale(lib):
+    s = _shape()
+    ok = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    assert lib.bl_attn_fwd(ctypes.byref(s), None, ok, ok, 0.1, ok, ok, None, None) == 1
+    assert lib.bl_attn_fwd(ctypes.byref(s), odd, ok, ok, 0.1, ok, ok, None, None) == 1
+    assert lib.bl_attn_fwd(ctypes.byref(s), ok, ok, ok, 0.0, ok, ok, None, None) == 1
+    assert lib.bl_attn_fwd(ctypes.byref(s), ok, ok, ok, float("nan"), ok, ok, None, None) == 1
+
+
+def test_mask_rejects_bad_negl_prob(lib):
+    from block_sparse_attention_fwd_gb300 import _lib
+    s = _shape()
+    ok = ctypes.c_void_p(0x10000)
+    L = _lib.Lists(ok, ok, ok, ok, ok, None)
+    for p in (-0.1, 1.0, 1.5, float("nan")):
+        assert lib.bl_mask_from_stats(ctypes.byref(s), ok, ok, p, ctypes.byref(L), None) == 1
+    L2 = _lib.Lists(ok, None, ok, ok, ok, None)
+    assert lib.bl_mask_from_stats(ctypes.byref(s), ok, ok, 0.05, ctypes.byref(L2), None) == 1
+
+
+def test_bwd_rejects_small_workspace(lib):
+    from block_sparse_attention_fwd_gb300 import _lib
+    s = _shape()
+    ok = ctypes.c_void_p(0x10000)
+    need = _lib.bwd_workspace_bytes(s)
+    r = lib.bl_attn_bwd(ctypes.byref(s), ok, ok, ok, ok, ok, ok, 0.125, None, ok, ok, ok,
+                        ok, need - 1, None)
+    assert r == 4
+    r = lib.bl_attn_bwd(ctypes.byref(s), ok, ok, ok, ok, ok, ok, 0.125, None, ok, ok, ok,
+                        None, need, None)
+    assert r == 4
+
+
+def test_status_strings(lib):
+    for c in range(7):
+        assert lib.bl_status_string(c)
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "block_sparse_attention_fwd_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", src, re.M), f

@@ -1,0 +1,143 @@
+"""GPU parity of the whole hot path against the fp64 oracle, element by
+element, on cases the oracle finishes in seconds (several tiles, ragged
+tails, GQA, both head dims, both tile sizes).  Every call goes through the
+C ABI binding."""
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_attention_fwd_gb300 import inputs
+from oracle import attention as A
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    (inputs.WORKLOADS["tiny_n256_d64"], 0.0),
+    (inputs.WORKLOADS["tiny_n256_d64"], 0.05),
+    (inputs.custom("ragged_n1000_d128_gqa", B=2, n=1000, H=4, Hk=2, d=128, run=48,
+                   clusters=8, alpha=3.0), 0.05),
+    (inputs.custom("ragged_n777_d64_t64", B=1, n=777, H=2, Hk=1, d=64, block_q=64,
+                   block_k=64, run=32, clusters=6, alpha=2.5), 0.1),
+    (inputs.custom("mixed_n640_d128_q64k128", B=1, n=640, H=2, Hk=2, d=128, block_q=64,
+                   block_k=128, run=40, clusters=5, alpha=3.0), 0.05),
+    (inputs.custom("ragged_n300_d128_t128", B=1, n=300, H=3, Hk=1, d=128, run=16,
+                   clusters=4, alpha=2.0), 0.02),
+    (inputs.WORKLOADS["clustered_n4096_d64"], 0.05),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _ids(c):
+    return f"{c[0].name}-negl{c[1]}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_hot_path_matches_oracle(case):
+    w, negl = case
+    from block_sparse_attention_fwd_gb300 import _lib
+    q, k, v, go = inputs.generate(w, seed=0)
+    scale = w.scale
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+
+    # ---- forward + statistics
+    qd, kd, vd, o, lse, stats = U.gpu_forward(shape, q, k, v, scale)
+    O, L, S = U.oracle_forward(q, k, v, scale, w.block_q, w.block_k)
+    assert U.rel_l2(U.cpu(o), O) <= U.REL_L2
+    assert np.abs(U.cpu(lse) - L).max() <= U.LSE_ABS
+    err, nchk, small_ok = U.compare_stats(U.cpu(stats), S, L, w.n)
+    assert nchk > 0 and err <= U.STATS_ABS and small_ok, (err, small_ok)
+    # rows past n hold -inf
+    pad = U.cpu(stats)[..., w.n:]
+    assert pad.size == 0 or np.all(pad == -np.inf)
+
+    # ---- mask: bit-exact given the GPU's own statistics
+    lists = U.gpu_mask(shape, stats, lse, negl)
+    ref_on_gpu_stats = U.oracle_mask(U.cpu(stats), U.cpu(lse), w.n, w.block_q, w.block_k, negl)
+    U.assert_lists_equal(lists, ref_on_gpu_stats)
+    own = U.oracle_mask(S, L, w.n, w.block_q, w.block_k, negl)
+    agree = float((U.cpu(lists["mask"]) == own["mask"]).mean())
+    assert agree >= 0.999, agree
+    if negl == 0.0:
+        assert np.all(own["mask"] == 1)
+
+    # ---- backward with the oracle's own mask on both sides
+    ol = U.lists_to_device(own)
+    gq, gk, gv, status = U.gpu_backward(shape, qd, kd, vd, o, go, lse, scale, ol)
+    assert status == 0
+    Ob = A.as_stored_output(O)
+    rq, rk, rv = A.backward(q, k, v, Ob, go, L, scale, own["mask"], w.block_q, w.block_k)
+    for name, a, b in (("G_Q", gq, rq), ("G_K", gk, rk), ("G_V", gv, rv)):
+        e = U.rel_l2(U.cpu(a), b)
+        assert e <= U.REL_L2, (name, e)
+
+    # ---- dense backward (lists = NULL) against the oracle's dense gradients
+    dq2, dk2, dv2, status = U.gpu_backward(shape, qd, kd, vd, o, go, lse, scale, None)
+    assert status == 0
+    dq, dk, dv = A.backward(q, k, v, Ob, go, L, scale)
+    for name, a, b in (("G_Q", dq2, dq), ("G_K", dk2, dk), ("G_V", dv2, dv)):
+        e = U.rel_l2(U.cpu(a), b)
+        assert e <= U.REL_L2, (name, e)
+    if negl == 0.0:
+        # negl_prob = 0 keeps every tile: the listed backward equals the dense one
+        for a, b in ((gq, dq2), (gk, dk2), (gv, dv2)):
+            assert torch.equal(a, b)
+
+
+def test_gpu_mask_on_planted_statistics():
+    """Hand-built statistics with exact ties, -inf tiles and a NaN tile."""
+    from block_sparse_attention_fwd_gb300 import _lib
+    B, H, n, b = 1, 2, 256, 64
+    shape = _lib.make_shape(B, n, H, H, 64, b, b)
+    rng = np.random.default_rng(7)
+    T = n // b
+    st = np.log(rng.dirichlet(np.full(T, 0.3), size=(B, H, n)).astype(np.float64))
+    st = np.transpose(st, (0, 1, 3, 2)).astype(np.float32).copy()   # [B,H,T_c,n]
+    st[0, 0, 1, :] = st[0, 0, 0, :]                                  # ties
+    st[0, 1, 2, :] = -np.inf                                         # empty tile
+    st[0, 1, 3, 5] = np.nan                                          # NaN weight
+    lse = np.zeros((B, H, n), dtype=np.float32)
+    for negl in (0.0, 0.01, 0.3, 0.9):
+        lists = _lib.alloc_lists(shape, "cuda")
+        _lib.mask_from_stats(shape, torch.from_numpy(st).cuda(), torch.from_numpy(lse).cuda(),
+                             negl, lists)
+        ref = U.oracle_mask(st, lse, n, b, b, negl)
+        U.assert_lists_equal(lists, ref)
+        assert int(lists["nan_count"].item()) == ref["nan_count"] == 1
+
+
+def test_corrupt_list_entry_is_reported_not_faulted():
+    from block_sparse_attention_fwd_gb300 import _lib
+    w = inputs.custom("corrupt", B=1, n=256, H=1, Hk=1, d=64, block_q=64, block_k=64)
+    q, k, v, go = inputs.generate(w)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    qd, kd, vd, o, lse, stats = U.gpu_forward(shape, q, k, v, w.scale)
+    lists = U.gpu_mask(shape, stats, lse, 0.05)
+    lists["q_idx"][0, 0, 0, 0] = 99          # out of range: T_r = 4
+    _, _, _, status = U.gpu_backward(shape, qd, kd, vd, o, go, lse, w.scale, lists)
+    assert status == 5                       # BL_ERR_CORRUPT_LISTS
+    lists["q_cnt"][0, 0, 1] = 1000
+    _, _, _, status = U.gpu_backward(shape, qd, kd, vd, o, go, lse, w.scale, lists)
+    assert status == 5
+
+
+def test_autograd_module_runs_the_chain():
+    from block_sparse_attention_fwd_gb300 import BLAttention
+    w = inputs.custom("module", B=1, n=512, H=2, Hk=1, d=64, run=32, clusters=4)
+    q, k, v, go = inputs.generate(w)
+    qd, kd, vd = (x.cuda().requires_grad_(True) for x in (q, k, v))
+    attn = BLAttention(negl_prob=0.05)
+    out, lse = attn(qd, kd, vd, return_softmax_lse=True)
+    out.backward(go.cuda())
+    O, L, S = A.forward(q, k, v, w.scale, block_q=128, block_k=128)
+    own = U.oracle_mask(S, L, w.n, 128, 128, 0.05)
+    rq, rk, rv = A.backward(q, k, v, A.as_stored_output(O), go, L, w.scale, own["mask"],
+                            128, 128)
+    assert U.rel_l2(U.cpu(out), O) <= U.REL_L2
+    for a, b in ((qd.grad, rq), (kd.grad, rk), (vd.grad, rv)):
+        assert U.rel_l2(U.cpu(a), b) <= U.REL_L2

@@ -132,3 +132,12 @@ def test_row_and_column_slices_agree_with_full():
                               L[0, 0], scale, m[0, 0], bq, bk, cols=cols)
     assert np.allclose(b, gk[0, cols, 0], atol=1e-13)
     assert np.allclose(c, gv[0, cols, 0], atol=1e-13)
+
+
+def test_stored_output_is_bf16_round_to_nearest_even():
+    # 1 + 2^-8 lies exactly between two bf16 values (spacing 2^-7): ties go to
+    # the even mantissa (1.0); 1 + 3*2^-8 rounds up to 1 + 2^-6.
+    x = np.array([[1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -3.0e38, 0.1]])
+    y = A.as_stored_output(x)
+    assert y[0, 0] == 1.0 and y[0, 1] == 1.0 + 2.0 ** -6
+    assert abs(y[0, 3] - 0.1) <= 0.1 * 2.0 ** -9
