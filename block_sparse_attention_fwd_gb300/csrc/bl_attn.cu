@@ -121,7 +121,8 @@ bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace, void
                                   (cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return BL_ERR_CUDA;
-  return host ? BL_ERR_CORRUPT_LISTS : BL_OK;
+  if (host & 2) return BL_ERR_TIMEOUT;
+  return (host & 1) ? BL_ERR_CORRUPT_LISTS : BL_OK;
 }
 
 const char* bl_status_string(bl_status status) {

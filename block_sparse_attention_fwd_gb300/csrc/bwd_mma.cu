@@ -317,7 +317,10 @@ cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void
                                                     (const __nv_bfloat16*)g_o, ws_D, sh);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (sh.d == 64 && sh.block_k == 64)
+  if (bwd_tc_supported(sh))
+    e = launch_bwd_tc(sh, q, k, v, g_o, lse, ws_D, q_idx, q_cnt, g_k, g_v, ws_dq, ws_status,
+                      scale, st);
+  else if (sh.d == 64 && sh.block_k == 64)
     e = launch_dkdv_t<64, 64>(sh, q, k, v, g_o, lse, ws_D, q_idx, q_cnt, g_k, g_v, ws_dq, ws_status, scale, st);
   else if (sh.d == 64 && sh.block_k == 128)
     e = launch_dkdv_t<64, 128>(sh, q, k, v, g_o, lse, ws_D, q_idx, q_cnt, g_k, g_v, ws_dq, ws_status, scale, st);

@@ -27,4 +27,11 @@ cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void
                        void* g_v, float* ws_D, float* ws_dq, int32_t* ws_status,
                        cudaStream_t st);
 
+// tcgen05 dK/dV/dQ pass for 128 x 128 tiles (head dim 64 or 128).
+bool bwd_tc_supported(const Shape& sh);
+cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const void* v,
+                          const void* g_o, const float* lse, const float* Dv,
+                          const int32_t* q_idx, const int32_t* q_cnt, void* g_k, void* g_v,
+                          float* dq_acc, int32_t* status, float scale, cudaStream_t st);
+
 }  // namespace bl

@@ -142,7 +142,8 @@ bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k,
                       size_t workspace_bytes, void* stream);
 
 /* Synchronises the stream and reads the status word a previous bl_attn_bwd
- * left in this workspace: BL_OK, or BL_ERR_CORRUPT_LISTS. */
+ * left in this workspace: BL_OK, BL_ERR_CORRUPT_LISTS, or BL_ERR_TIMEOUT (a
+ * bounded device-side wait gave up; the outputs of that call are invalid). */
 bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace,
                               void* stream);
 

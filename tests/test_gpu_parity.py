@@ -111,9 +111,10 @@ def test_gpu_mask_on_planted_statistics():
         assert int(lists["nan_count"].item()) == ref["nan_count"] == 1
 
 
-def test_corrupt_list_entry_is_reported_not_faulted():
+@pytest.mark.parametrize("tile,d", [(64, 64), (128, 128), (128, 64)])
+def test_corrupt_list_entry_is_reported_not_faulted(tile, d):
     from block_sparse_attention_fwd_gb300 import _lib
-    w = inputs.custom("corrupt", B=1, n=256, H=1, Hk=1, d=64, block_q=64, block_k=64)
+    w = inputs.custom("corrupt", B=1, n=4 * tile, H=1, Hk=1, d=d, block_q=tile, block_k=tile)
     q, k, v, go = inputs.generate(w)
     shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
     qd, kd, vd, o, lse, stats = U.gpu_forward(shape, q, k, v, w.scale)
