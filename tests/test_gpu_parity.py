@@ -84,9 +84,11 @@ def test_hot_path_matches_oracle(case):
         e = U.rel_l2(U.cpu(a), b)
         assert e <= U.REL_L2, (name, e)
     if negl == 0.0:
-        # negl_prob = 0 keeps every tile: the listed backward equals the dense one
-        for a, b in ((gq, dq2), (gk, dk2), (gv, dv2)):
-            assert torch.equal(a, b)
+        # negl_prob = 0 keeps every tile: the listed backward is the dense one.
+        # G_K and G_V are accumulated in a fixed order and match bit for bit;
+        # G_Q sums fp32 atomic adds whose order varies from run to run.
+        assert torch.equal(gk, dk2) and torch.equal(gv, dv2)
+        assert U.rel_l2(U.cpu(gq), U.cpu(dq2)) <= 1e-3
 
 
 def test_gpu_mask_on_planted_statistics():
