@@ -20,7 +20,8 @@ BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "B
 
 # Every symbol include/bl_attn.h declares (checked by the CPU test suite).
 EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
-           "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string")
+           "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
+           "bl_attn_bwd_noalloc")
 
 
 class Shape(ctypes.Structure):
@@ -65,6 +66,8 @@ def load():
     lib.bl_mask_from_stats.restype = ctypes.c_int
     lib.bl_attn_bwd.argtypes = [S, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P, P, Z, P]
     lib.bl_attn_bwd.restype = ctypes.c_int
+    lib.bl_attn_bwd_noalloc.argtypes = [S, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P, P]
+    lib.bl_attn_bwd_noalloc.restype = ctypes.c_int
     lib.bl_bwd_check_status.argtypes = [S, P, P]
     lib.bl_bwd_check_status.restype = ctypes.c_int
     lib.bl_status_string.argtypes = [ctypes.c_int]
@@ -191,3 +194,21 @@ def attn_bwd(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, workspace
 def bwd_check_status(shape, workspace) -> int:
     return int(load().bl_bwd_check_status(ctypes.byref(shape), _ptr(workspace),
                                           _stream(workspace.device)))
+
+
+def attn_bwd_noalloc(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v):
+    """bl_attn_bwd_noalloc: the backward with the library's fixed device scratch
+    instead of a workspace (for callers that cannot allocate device memory)."""
+    B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
+    for t, nm, sh in ((q, "q", (B, n, H, d)), (k, "k", (B, n, Hk, d)), (v, "v", (B, n, Hk, d)),
+                      (o, "o", (B, n, H, d)), (g_o, "g_o", (B, n, H, d)),
+                      (g_q, "g_q", (B, n, H, d)), (g_k, "g_k", (B, n, Hk, d)),
+                      (g_v, "g_v", (B, n, Hk, d))):
+        _need(t, torch.bfloat16, sh, nm)
+    _need(lse, torch.float32, (B, H, n), "lse")
+    ls = _lists_struct(lists) if lists is not None else None
+    code = load().bl_attn_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                      _ptr(g_o), _ptr(lse), float(scale),
+                                      ctypes.byref(ls) if ls is not None else None,
+                                      _ptr(g_q), _ptr(g_k), _ptr(g_v), _stream(q.device))
+    _check("bl_attn_bwd_noalloc", code)

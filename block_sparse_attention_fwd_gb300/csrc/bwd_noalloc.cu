@@ -1,0 +1,85 @@
+// bl_attn_bwd_noalloc: the block-sparse backward without a caller-supplied
+// workspace, for callers that cannot call cudaMalloc themselves -- for
+// example a host runtime that owns all device memory through its own pool
+// and lets no library allocate behind its back, or a latency-critical caller
+// that cannot accept the implicit device synchronisation of cudaMalloc.
+//
+// The scratch the backward needs (D = rowsum(G_O * O), the fp32 dQ
+// accumulator and the status word) lives in one fixed array in device
+// global memory, BL_NOALLOC_SCRATCH_BYTES long, that every GPU loading this
+// library holds until the process exits.  The call itself allocates
+// nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+#include <math.h>
+
+#include <mutex>
+
+#include "../../include/bl_attn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// The scratch array.  In host code this name is only a host-side stand-in
+// for the symbol: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BL_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).  nullptr on failure.
+void* scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* k,
+                                         const void* v, const void* o, const void* g_o,
+                                         const float* lse, float scale, const bl_lists* lists,
+                                         void* g_q, void* g_k, void* g_v, void* stream) {
+  if (!shape) return BL_ERR_INVALID_ARG;
+  const size_t need = bl_bwd_workspace_bytes(shape);
+  if (need == 0)  // invalid shape: bl_attn_bwd returns its shape error before any launch
+    return bl_attn_bwd(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, nullptr, 0,
+                       stream);
+  if (need > (size_t)BL_NOALLOC_SCRATCH_BYTES) return BL_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k, v, o, g_o, lse, g_q, g_k, g_v};
+  for (const void* p : ptrs)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return BL_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
+  if (lists && (!lists->q_idx || !lists->q_cnt)) return BL_ERR_INVALID_ARG;
+  unsigned char* ws = static_cast<unsigned char*>(scratch_address());
+  if (!ws) return BL_ERR_CUDA;
+
+  bl::Shape sh;
+  sh.B = shape->B; sh.n = shape->n; sh.H = shape->H; sh.Hk = shape->Hk; sh.d = shape->d;
+  sh.block_q = shape->block_q; sh.block_k = shape->block_k;
+  sh.T_r = (sh.n + sh.block_q - 1) / sh.block_q;
+  sh.T_c = (sh.n + sh.block_k - 1) / sh.block_k;
+  sh.n_pad = (int64_t)sh.T_r * sh.block_q;
+  // Same layout as the workspace of bl_attn_bwd.  launch_bwd zeroes the dQ
+  // accumulator and the status word on the stream before its kernels run, and
+  // the preprocessing kernel writes every D entry, so nothing left by an
+  // earlier call leaks into this one.
+  const size_t d_bytes = round256((size_t)sh.B * sh.H * sh.n * sizeof(float));
+  const size_t dq_bytes = (size_t)sh.B * sh.n * sh.H * sh.d * sizeof(float);
+  float* ws_D = reinterpret_cast<float*>(ws);
+  float* ws_dq = reinterpret_cast<float*>(ws + d_bytes);
+  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + d_bytes + dq_bytes);
+  cudaError_t e = bl::launch_bwd(sh, q, k, v, o, g_o, lse, scale, lists ? lists->q_idx : nullptr,
+                                 lists ? lists->q_cnt : nullptr, g_q, g_k, g_v, ws_D, ws_dq,
+                                 ws_status, (cudaStream_t)stream);
+  return e == cudaSuccess ? BL_OK : BL_ERR_CUDA;
+}

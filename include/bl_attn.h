@@ -147,6 +147,33 @@ bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k,
 bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace,
                               void* stream);
 
+/* Size of the fixed device scratch array behind bl_attn_bwd_noalloc: 32 MiB
+ * on every GPU that loads the library, held until the process exits. */
+#define BL_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* bl_attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory themselves (for instance a host runtime that owns every byte
+ * of device memory through its own pool, or a latency-critical caller that
+ * cannot afford cudaMalloc's implicit synchronisation).  The BackLite pages
+ * have no counterpart: this is a deployment convenience of this library.
+ *
+ * Same arguments, results and errors as bl_attn_bwd, except that the
+ * scratch (D, the fp32 dQ accumulator, the status word) lives in a fixed
+ * file-scope device array of BL_NOALLOC_SCRATCH_BYTES.  The call allocates
+ * nothing.  A shape whose bl_bwd_workspace_bytes exceeds that size is
+ * rejected with BL_ERR_WORKSPACE before any launch.  The first call on each
+ * device looks the array's device address up (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array and it keeps the last call's contents (each call
+ * clears what must start at zero), so calls that overlap on the GPU -- on
+ * different streams, or from different threads -- race and must be
+ * serialised by the caller.  The status word cannot be read back: list
+ * entries out of range are skipped exactly as in bl_attn_bwd. */
+bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* k,
+                              const void* v, const void* o, const void* g_o,
+                              const float* lse, float scale, const bl_lists* lists,
+                              void* g_q, void* g_k, void* g_v, void* stream);
+
 /* Static description of a status code. */
 const char* bl_status_string(bl_status status);
 
