@@ -47,29 +47,67 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """SM clocks, power and throttle reasons sampled during the timed region.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads NVML through ctypes from a background thread (no child processes, so
+    nothing forks the CUDA process while kernels run); falls back to
+    nvidia-smi only if libnvidia-ml cannot be loaded.  Only reads settings."""
 
-    def __init__(self, gpu_id: str):
-        self.idx = gpu_id
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_id: str, period_s: float = 0.05):
+        self.gpu_id = gpu_id
+        self.period = period_s
         self.rows = []
         self._stop = threading.Event()
         self._t = None
+        self._nvml = None
+        self._dev = None
+        self.max_mhz = None
+        try:
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() == 0:
+                dev = ctypes.c_void_p()
+                if lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(dev)) == 0:
+                    self._nvml, self._dev = lib, dev
+                    mx = ctypes.c_uint()
+                    if lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = float(mx.value)
+        except OSError:
+            self._nvml = None
+
+    def _sample_nvml(self):
+        import ctypes
+        lib, dev = self._nvml, self._dev
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        lib.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(clk))          # NVML_CLOCK_SM
+        lib.nvmlDeviceGetPowerUsage(dev, ctypes.byref(pw))
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(dev, ctypes.byref(rs))
+        return float(clk.value), pw.value / 1000.0, int(rs.value)
+
+    def _sample_smi(self):
+        q = ("clocks.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap,clocks.max.sm")
+        out = subprocess.run(["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={q}",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=5).stdout.strip().split(",")
+        bits = [0x8, 0x40, 0x20, 0x4]
+        rs = sum(b for b, v in zip(bits, out[2:6]) if v.strip().lower() == "active")
+        self.max_mhz = float(out[6])
+        return float(out[0]), float(out[1]), rs
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                out = subprocess.run(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                      "--format=csv,noheader,nounits"], capture_output=True,
-                                     text=True, timeout=5).stdout.strip()
-                if out:
-                    self.rows.append([x.strip() for x in out.split(",")])
+                self.rows.append(self._sample_nvml() if self._nvml else self._sample_smi())
             except Exception:
                 pass
-            self._stop.wait(0.2)
+            self._stop.wait(self.period)
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
@@ -82,15 +120,13 @@ class ClockSampler:
 
     def summary(self):
         if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4)
-                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"]}
+        reasons = sorted({name for _, _, r in self.rows for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": max(r[1] for r in self.rows),
+                "source": "nvml" if self._nvml else "nvidia-smi"}
 
 
 def _smi_id(dev):

@@ -407,41 +407,6 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
   if (warp == 1) tmem_free(tmem, C::T_COLS);
 }
 
-// ------------------------------------------------------------------ host side
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-  static EncodeFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  }
-  return fn;
-}
-
-// BSHD bf16 tensor [B][n][heads][d] as a 4-D map (d, heads, n, B); box of 64
-// elements of d x 1 head x `rows` tokens x 1 batch, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows) {
-  EncodeFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)n, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
-                           (cuuint64_t)n * heads * d * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, const void* g_o,
                      const float* lse, const float* Dv, const int32_t* q_idx,
@@ -449,8 +414,8 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
                      float scale, cudaStream_t st) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv, mg;
-  if (!make_map(&mq, q, sh.B, sh.n, sh.H, D, 64) || !make_map(&mg, g_o, sh.B, sh.n, sh.H, D, 64) ||
-      !make_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) || !make_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128))
+  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 64) || !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 64) ||
+      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) || !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
   auto kern = bwd_tc_kernel<D>;

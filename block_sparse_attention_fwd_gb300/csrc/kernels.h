@@ -1,6 +1,7 @@
 // Host-side launchers of the bl_attn kernels (internal to libbl_attn.so).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,5 +34,15 @@ cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const v
                           const void* g_o, const float* lse, const float* Dv,
                           const int32_t* q_idx, const int32_t* q_cnt, void* g_k, void* g_v,
                           float* dq_acc, int32_t* status, float scale, cudaStream_t st);
+
+// tcgen05 forward with tile statistics for 128 x 128 tiles (head dim 64 or 128).
+bool fwd_tc_supported(const Shape& sh);
+cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
+                          float* lse, float* stats, int32_t* status, float scale,
+                          cudaStream_t st);
+
+// 4-D TMA map of a BSHD bf16 tensor [B][n][heads][d]: box of 64 elements of d
+// x 1 head x `rows` tokens x 1 batch, 128-byte swizzle, out-of-range reads 0.
+bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows);
 
 }  // namespace bl

@@ -89,6 +89,11 @@ WORKLOADS = {
                                   d=128, block_q=128, block_k=128,
                                   negl_probs=(0.05,), kind="grid", alpha=3.0,
                                   grid=(21, 30, 52), patch=(3, 6, 8)),
+    # the video grid with 8 heads: same per-head structure, a small case for profiling
+    "video_n32760_d128_h8": Workload("video_n32760_d128_h8", B=1, n=32760, H=8, Hk=8,
+                                     d=128, block_q=128, block_k=128,
+                                     negl_probs=(0.05,), kind="grid", alpha=3.0,
+                                     grid=(21, 30, 52), patch=(3, 6, 8)),
     "long_n131072_d128": Workload("long_n131072_d128", B=1, n=131072, H=32, Hk=8,
                                   d=128, block_q=128, block_k=128,
                                   negl_probs=(0.05,), kind="runs", alpha=3.0,
