@@ -18,7 +18,7 @@
 // Warp roles (12 warps):
 //   warp 0      TMA producer: K_j, V_j once; then per half Q and dO (4-D
 //               tensor maps, 128-byte swizzle, out-of-range rows read as 0)
-//               into a 3-slot ring, plus the half's LSE and D rows.
+//               into a 2-slot ring, plus the half's LSE and D rows.
 //   warp 1      MMA issuer (one thread) and TMEM owner.  Per half h it issues
 //               S^T_h, dP^T_h, then the gradient MMAs of half h-1 (dV, dK and,
 //               after the second half of a tile, dQ), so the softmax of h
@@ -26,8 +26,11 @@
 //   warps 4-7   softmax warpgroup: thread = key row; reads S^T/dP^T rows from
 //               TMEM, writes P^T and dS^T (bf16, swizzled) to shared memory;
 //               at the end writes dK, dV.
+//   warps 2-3   at start: copy this CTA's tile lists into shared memory.
 //   warps 8-11  dQ warpgroup: thread = query row; drains the dQ tile from
-//               TMEM into the fp32 accumulator with vector atomics.
+//               TMEM through a 128-byte-swizzled staging buffer (32 columns at
+//               a time) into the fp32 accumulator with TMA bulk reduce-adds,
+//               which the L2 applies as whole-line reductions.
 // All hand-offs are mbarriers; every wait is bounded (tc.cuh).
 #include "common.cuh"
 #include "kernels.h"
@@ -41,22 +44,29 @@ using namespace tc;
 
 template <int D>
 struct Cfg {
-  static constexpr int BK = 128, HQ = 64, NS = 3;
+  static constexpr int BK = 128, HQ = 64, NS = 2;
   static constexpr int CHK = D / 64;              // 64-element chunks along d
   static constexpr int KV_CHUNK = BK * 128;       // [128 rows][128 B]
   static constexpr int QH_CHUNK = HQ * 128;       // [64 rows][128 B]
   static constexpr int KV_BYTES = KV_CHUNK * CHK;
   static constexpr int QH_BYTES = QH_CHUNK * CHK;
   static constexpr int P_BYTES = BK * HQ * 2;     // [128 keys][64 q] bf16
+  static constexpr int STAGE_BYTES = 128 * 128;   // dQ staging: [128 rows][32 fp32]
+  static constexpr int LIST_CAP = 2048;           // cached list entries per CTA
+  static constexpr int GMAX = 32;                 // heads per GQA group with cached lists
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
   static constexpr int OFF_Q = OFF_V + KV_BYTES;
   static constexpr int OFF_G = OFF_Q + NS * QH_BYTES;
   static constexpr int OFF_P = OFF_G + NS * QH_BYTES;
   static constexpr int OFF_S = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_L = OFF_S + 2 * P_BYTES;   // NS x 64 floats: lse*log2e
-  static constexpr int OFF_D = OFF_L + NS * HQ * 4;   // NS x 64 floats: D
-  static constexpr int BYTES = OFF_D + NS * HQ * 4;
+  static constexpr int OFF_STAGE = OFF_S + 2 * P_BYTES;
+  static constexpr int OFF_L = OFF_STAGE + STAGE_BYTES;   // NS x 64 floats: lse*log2e
+  static constexpr int OFF_D = OFF_L + NS * HQ * 4;       // NS x 64 floats: D
+  static constexpr int OFF_LIST = OFF_D + NS * HQ * 4;    // LIST_CAP ints
+  static constexpr int OFF_LCNT = OFF_LIST + LIST_CAP * 4;  // GMAX ints
+  static constexpr int OFF_LBASE = OFF_LCNT + GMAX * 4;     // GMAX ints
+  static constexpr int BYTES = OFF_LBASE + GMAX * 4;
   static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 128 + D, T_DK = 128 + 2 * D;
   static constexpr uint32_t T_COLS = 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, 64, false, false);
@@ -65,16 +75,20 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t kv, full[3], empty[3], s, p, pfree[2], dsfree, dqready, dqfree, acc;
+  uint64_t kv, full[2], empty[2], s, p, pfree[2], dsfree, dqready, dqfree, acc;
 };
 
 // Iterates the kept query tiles of key tile j over the heads of one GQA group,
-// identically in every role.  Returns false when done.
+// identically in every role.  Reads the lists from shared memory when they
+// were cached there (s_list/s_cnt/s_base), else from global memory.
 struct Walk {
   const int32_t* q_idx;
   const int32_t* q_cnt;
   const Shape* sh;
   int j, b, hk, G;
+  const int32_t* s_list;   // nullptr: not cached
+  const int32_t* s_cnt;
+  const int32_t* s_base;
   int gi = 0, li = 0, cnt = -1;
   int h = 0, i = 0;
   bool corrupt = false;
@@ -84,10 +98,14 @@ struct Walk {
       h = hk * G + gi;
       const int64_t bh = (int64_t)b * sh->H + h;
       if (cnt < 0) {
-        cnt = q_cnt ? q_cnt[bh * sh->T_c + j] : sh->T_r;
-        if (cnt < 0 || cnt > sh->T_r) {
-          corrupt = true;
-          cnt = 0;
+        if (s_list) {
+          cnt = s_cnt[gi];
+        } else {
+          cnt = q_cnt ? q_cnt[bh * sh->T_c + j] : sh->T_r;
+          if (cnt < 0 || cnt > sh->T_r) {
+            corrupt = true;
+            cnt = 0;
+          }
         }
         li = 0;
       }
@@ -96,7 +114,10 @@ struct Walk {
         cnt = -1;
         continue;
       }
-      i = q_idx ? q_idx[(bh * sh->T_c + j) * (int64_t)sh->T_r + li] : li;
+      if (s_list)
+        i = s_list[s_base[gi] + li];
+      else
+        i = q_idx ? q_idx[(bh * sh->T_c + j) * (int64_t)sh->T_r + li] : li;
       ++li;
       if (i < 0 || i >= sh->T_r) {
         corrupt = true;
@@ -113,7 +134,7 @@ template <int D>
 __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-    const float* __restrict__ lse, const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
+    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse, const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
     const int32_t* __restrict__ q_cnt, __nv_bfloat16* __restrict__ g_k,
     __nv_bfloat16* __restrict__ g_v, float* __restrict__ dq_acc, int32_t* __restrict__ status,
     Shape sh, float scale, float scale_log2) {
@@ -123,7 +144,8 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
                                            ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_fail;
+  __shared__ int s_fail, s_cached;
+  __shared__ int s_drain_ok[4];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
@@ -147,6 +169,42 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&s_tmem, C::T_COLS);
+  int32_t* s_list = reinterpret_cast<int32_t*>(sm + C::OFF_LIST);
+  int32_t* s_lcnt = reinterpret_cast<int32_t*>(sm + C::OFF_LCNT);
+  int32_t* s_lbase = reinterpret_cast<int32_t*>(sm + C::OFF_LBASE);
+  if (warp == 2 || warp == 3) {
+    // copy this CTA's lists (all heads of the GQA group) into shared memory
+    const int t = threadIdx.x - 64;
+    const bool can = q_idx != nullptr && G <= C::GMAX;
+    if (can) {
+      for (int g = t; g < G; g += 64) {
+        int c = q_cnt[((int64_t)b * sh.H + hk * G + g) * sh.T_c + j];
+        if (c < 0 || c > sh.T_r) {
+          c = 0;
+          atomicOr(status, kStatusCorrupt);
+        }
+        s_lcnt[g] = c;
+      }
+    }
+    named_sync(2, 64);
+    if (t == 0) {
+      int tot = 0;
+      if (can)
+        for (int g = 0; g < G; ++g) {
+          s_lbase[g] = tot;
+          tot += s_lcnt[g];
+        }
+      s_cached = can && tot <= C::LIST_CAP;
+    }
+    named_sync(2, 64);
+    if (s_cached) {
+      for (int g = 0; g < G; ++g) {
+        const int32_t* src =
+            q_idx + (((int64_t)b * sh.H + hk * G + g) * sh.T_c + j) * (int64_t)sh.T_r;
+        for (int li = t; li < s_lcnt[g]; li += 64) s_list[s_lbase[g] + li] = src[li];
+      }
+    }
+  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -156,7 +214,8 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
     atomicOr(&s_fail, 1);
     atomicOr(status, kStatusTimeout);
   };
-  Walk walk{q_idx, q_cnt, &sh, j, b, hk, G};
+  const bool cached = s_cached != 0;
+  Walk walk{q_idx, q_cnt, &sh, j, b, hk, G, cached ? s_list : nullptr, s_lcnt, s_lbase};
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -373,32 +432,47 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain
     const int q4 = warp & 3;
+    const int dt = threadIdx.x - 256;              // 0..127, = row within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    uint8_t* stage = sm + C::OFF_STAGE;
+    uint8_t* srow = stage + dt * 128;
     int u = 0;
     bool ok = true;
     while (ok && walk.next()) {
-      ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.dqready, u & 1));
+      // the four drain warps agree on success before any named barrier
+      const bool w_ok =
+          __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.dqready, u & 1));
+      if (lane == 0) s_drain_ok[q4] = w_ok;
+      named_sync(1, 128);
+      ok = s_drain_ok[0] && s_drain_ok[1] && s_drain_ok[2] && s_drain_ok[3];
+      named_sync(1, 128);
       if (!ok) break;
       fence_after_sync();
-      const int row = walk.i * 128 + q4 * 32 + lane;
-      float* dst = dq_acc + (((int64_t)b * sh.n + row) * sh.H + walk.h) * D;
-#pragma unroll
+#pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t a[32];
         tmem_ld32(lane_base + C::T_DQ + c0, a);
         tmem_ld_wait();
-        if (row < sh.n) {
+        if (c0 + 32 == D) {          // the dQ columns of TMEM are free again
+          fence_before_sync();
+          mbar_arrive(&bars.dqfree);
+        }
+        if (dt == 0) bulk_wait_read0();   // previous reduce has read the staging rows
+        named_sync(1, 128);
 #pragma unroll
-          for (int x = 0; x < 32; x += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + c0 + x),
-                      make_float4(__uint_as_float(a[x]), __uint_as_float(a[x + 1]),
-                                  __uint_as_float(a[x + 2]), __uint_as_float(a[x + 3])));
+        for (int x = 0; x < 8; ++x)
+          *reinterpret_cast<uint4*>(srow + ((x ^ (dt & 7)) << 4)) =
+              make_uint4(a[4 * x], a[4 * x + 1], a[4 * x + 2], a[4 * x + 3]);
+        fence_async_smem();
+        named_sync(1, 128);
+        if (dt == 0) {
+          tma_reduce_add_4d(&tm_dq, stage, c0, walk.h, walk.i * 128, b);
+          bulk_commit();
         }
       }
-      fence_before_sync();
-      mbar_arrive(&bars.dqfree);
       ++u;
     }
+    if (dt == 0) bulk_wait0();
     if (!ok && lane == 0) fail();
   }
 
@@ -413,16 +487,17 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
                      const int32_t* q_cnt, void* g_k, void* g_v, float* dq_acc, int32_t* status,
                      float scale, cudaStream_t st) {
   using C = Cfg<D>;
-  CUtensorMap mq, mk, mv, mg;
+  CUtensorMap mq, mk, mv, mg, md;
   if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 64) || !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 64) ||
-      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) || !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128))
+      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) || !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
+      !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
   auto kern = bwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(sh.T_c, sh.Hk, sh.B);
-  kern<<<grid, 384, smem, st>>>(mq, mk, mv, mg, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
+  kern<<<grid, 384, smem, st>>>(mq, mk, mv, mg, md, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
                                 (__nv_bfloat16*)g_v, dq_acc, status, sh, scale, scale * kLog2e);
   return cudaGetLastError();
 }

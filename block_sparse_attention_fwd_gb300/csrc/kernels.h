@@ -45,4 +45,9 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
 // x 1 head x `rows` tokens x 1 batch, 128-byte swizzle, out-of-range reads 0.
 bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows);
 
+// The same for an fp32 BSHD tensor, box of 32 elements of d (128 bytes) x 1
+// head x `rows` tokens, 128-byte swizzle: the target of dQ reduce-adds.
+bool make_bshd_map_f32(CUtensorMap* m, const void* base, int B, int n, int heads, int d,
+                       int rows);
+
 }  // namespace bl

@@ -44,4 +44,19 @@ bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_bshd_map_f32(CUtensorMap* m, const void* base, int B, int n, int heads, int d,
+                       int rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)n, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4,
+                           (cuuint64_t)n * heads * d * 4};
+  cuuint32_t box[4] = {32, 1, (cuuint32_t)rows, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace bl
