@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv, 1);
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&bars.full[s], 32);
+      mbar_init(&bars.full[s], 33);
       mbar_init(&bars.empty[s], 1);
     }
     mbar_init(&bars.s, 1);
@@ -235,19 +235,19 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
       const int64_t bh = (int64_t)b * sh.H + walk.h;
       for (int half = 0; half < 2; ++half, ++hc) {
         const int s = hc % C::NS;
-        if (failed(&s_fail) || !mbar_wait(&bars.empty[s], ((hc / C::NS) & 1) ^ 1)) {
-          if (lane == 0) fail();
-          goto producer_done;
-        }
         const int r0 = walk.i * 128 + half * 64;
-        float* sl = reinterpret_cast<float*>(sm + C::OFF_L) + s * 64;
-        float* sd = reinterpret_cast<float*>(sm + C::OFF_D) + s * 64;
+        // start the LSE and D loads of this half before waiting for its slot
+        float lv[2], dv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int r = r0 + lane + 32 * e;
           const bool ok = r < sh.n;
-          sl[lane + 32 * e] = ok ? lse[bh * sh.n + r] * kLog2e : INFINITY;
-          sd[lane + 32 * e] = ok ? Dv[bh * sh.n + r] : 0.f;
+          lv[e] = ok ? lse[bh * sh.n + r] * kLog2e : INFINITY;
+          dv[e] = ok ? Dv[bh * sh.n + r] : 0.f;
+        }
+        if (failed(&s_fail) || !mbar_wait(&bars.empty[s], ((hc / C::NS) & 1) ^ 1)) {
+          if (lane == 0) fail();
+          goto producer_done;
         }
         if (lane == 0) {
           mbar_expect_tx(&bars.full[s], 2 * C::QH_BYTES);
@@ -257,9 +257,15 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
             tma_load_4d(sm + C::OFF_G + s * C::QH_BYTES + c * C::QH_CHUNK, &tm_g, &bars.full[s],
                         c * 64, walk.h, r0, b);
           }
-        } else {
-          mbar_arrive(&bars.full[s]);
         }
+        float* sl = reinterpret_cast<float*>(sm + C::OFF_L) + s * 64;
+        float* sd = reinterpret_cast<float*>(sm + C::OFF_D) + s * 64;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          sl[lane + 32 * e] = lv[e];
+          sd[lane + 32 * e] = dv[e];
+        }
+        mbar_arrive(&bars.full[s]);   // with lane 0's expect_tx arrival: 33 per phase
       }
     }
     if (lane == 0 && walk.corrupt) atomicOr(status, kStatusCorrupt);
