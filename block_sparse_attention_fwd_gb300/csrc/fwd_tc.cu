@@ -11,16 +11,20 @@
 // more than 2^8 (in base-2 units), so the rescale of O in TMEM is rare; the
 // exponentials stay below 2^8 and the result is the same softmax.
 //
-// One CTA per (128-row query tile, head, batch).  TMEM: S double buffer
-// [0,128) and [128,256), O [256,256+d).  Warp roles (8 warps):
-//   warp 0     TMA producer: Q once, then K_j, V_j into a 2-stage ring.
-//   warp 1     MMA issuer (one thread), TMEM owner: S_j = Q K_j^T, then
-//              O += P_{j-1} V_{j-1}, so the softmax of tile j overlaps the PV
-//              product of tile j-1.
-//   warps 4-7  softmax warpgroup, thread = query row: reads S_j from TMEM,
-//              writes the tile statistic (one coalesced 512-byte row per key
-//              tile), P_j (bf16, 128-byte swizzled) to shared memory; at the
-//              end writes O = acc / l and LSE.
+// One CTA per (pair of 128-row query tiles A and B, head, batch).  TMEM:
+// S_A [0,128), S_B [128,256), O_A [256,256+d), O_B [256+d,256+2d).  P (bf16)
+// is written over the first 64 columns of its S and read from TMEM by the
+// P V product, so P never passes through shared memory.  Warp roles:
+//   warp 0     TMA producer: Q_A, Q_B once; K_j into a 3-stage ring and V_j
+//              into a 2-stage ring (V one key tile behind K).
+//   warp 1     MMA issuer (one thread), TMEM owner.  For key tile j and each
+//              query tile t: O_t += P_t(j) V_j, then S_t(j+1) = Q_t K_{j+1}^T,
+//              so while one softmax warpgroup works on its tile the tensor
+//              core runs the other tile's products.
+//   warps 4-7  softmax warpgroup of tile A, warps 8-11 of tile B; thread =
+//              query row: S row from TMEM, tile statistic (coalesced 512 B
+//              per key tile), P back into TMEM; at the end O = acc / l, LSE.
+// Every mbarrier wait is bounded (tc.cuh).
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -33,17 +37,14 @@ using namespace tc;
 
 template <int D>
 struct FCfg {
-  static constexpr int NS = 2;
+  static constexpr int NK = 3, NV = 2;                  // K and V ring stages
   static constexpr int CHK = D / 64;
   static constexpr int CHUNK = 128 * 128;               // [128 rows][128 B]
-  static constexpr int Q_BYTES = CHUNK * CHK;
-  static constexpr int KV_BYTES = CHUNK * CHK;
-  static constexpr int P_BYTES = 2 * CHUNK;             // [128 q][128 keys] bf16
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-  static constexpr int BYTES = OFF_P + 2 * P_BYTES;
+  static constexpr int TILE_BYTES = CHUNK * CHK;        // one 128 x d bf16 tile
+  static constexpr int OFF_Q = 0;                       // Q_A, Q_B
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+  static constexpr int BYTES = OFF_V + NV * TILE_BYTES;
   static constexpr uint32_t T_S = 0, T_O = 256, T_COLS = 512;
   static constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t ID_O = idesc_bf16(128, D, false, true);
@@ -51,17 +52,17 @@ struct FCfg {
 };
 
 struct FBars {
-  uint64_t q, kv_full[2], kv_empty[2], s_full[2], p_ready[2], p_free[2], o_step, o_done;
+  uint64_t q, k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], p_ready[2], o_done[2];
 };
 
 __device__ __forceinline__ bool failed(const int* f) { return *(volatile const int*)f != 0; }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) fwd_tc_kernel(
+__global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
-    float* __restrict__ lse, float* __restrict__ stats, int32_t* __restrict__ status, Shape sh,
-    float scale_log2) {
+    float* __restrict__ lse, float* __restrict__ stats, Shape sh, float scale_log2) {
   using C = FCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -71,21 +72,27 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (sh.H / sh.Hk);
   const int Tc = sh.T_c;
+  // the second tile of the last pair may lie wholly past the last query tile
+  const int ntile = min(2, sh.T_r - 2 * pair);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
-      mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_ready[s], 128);
-      mbar_init(&bars.p_free[s], 1);
+    for (int s = 0; s < C::NK; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
     }
-    mbar_init(&bars.o_step, 1);
-    mbar_init(&bars.o_done, 1);
+    for (int s = 0; s < C::NV; ++s) {
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_ready[t], 128);
+      mbar_init(&bars.o_done[t], 1);
+    }
     s_fail = 0;
     fence_mbar_init();
   }
@@ -94,10 +101,7 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
-  auto fail = [&]() {
-    atomicOr(&s_fail, 1);
-    if (status) atomicOr(status, kStatusTimeout);
-  };
+  auto fail = [&]() { atomicOr(&s_fail, 1); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -105,171 +109,187 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_expect_tx(&bars.q, C::Q_BYTES);
-      for (int c = 0; c < C::CHK; ++c)
-        tma_load_4d(sm + C::OFF_Q + c * C::CHUNK, &tm_q, &bars.q, c * 64, h, qt * 128, b);
-      for (int j = 0; j < Tc; ++j) {
-        const int s = j & 1;
-        if (failed(&s_fail) || !mbar_wait(&bars.kv_empty[s], ((j >> 1) & 1) ^ 1)) {
-          fail();
-          break;
+      mbar_expect_tx(&bars.q, ntile * C::TILE_BYTES);
+      for (int t = 0; t < ntile; ++t)
+        for (int c = 0; c < C::CHK; ++c)
+          tma_load_4d(sm + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK, &tm_q, &bars.q, c * 64,
+                      h, (2 * pair + t) * 128, b);
+      auto load_v = [&](int jv) -> bool {
+        const int sv = jv % C::NV;
+        if (!mbar_wait(&bars.v_empty[sv], ((jv / C::NV) & 1) ^ 1)) return false;
+        mbar_expect_tx(&bars.v_full[sv], C::TILE_BYTES);
+        for (int c = 0; c < C::CHK; ++c)
+          tma_load_4d(sm + C::OFF_V + sv * C::TILE_BYTES + c * C::CHUNK, &tm_v, &bars.v_full[sv],
+                      c * 64, hk, jv * 128, b);
+        return true;
+      };
+      bool ok = true;
+      for (int j = 0; ok && j <= Tc; ++j) {
+        if (j < Tc) {
+          const int sk = j % C::NK;
+          ok = !failed(&s_fail) && mbar_wait(&bars.k_empty[sk], ((j / C::NK) & 1) ^ 1);
+          if (!ok) break;
+          mbar_expect_tx(&bars.k_full[sk], C::TILE_BYTES);
+          for (int c = 0; c < C::CHK; ++c)
+            tma_load_4d(sm + C::OFF_K + sk * C::TILE_BYTES + c * C::CHUNK, &tm_k,
+                        &bars.k_full[sk], c * 64, hk, j * 128, b);
         }
-        mbar_expect_tx(&bars.kv_full[s], 2 * C::KV_BYTES);
-        for (int c = 0; c < C::CHK; ++c) {
-          tma_load_4d(sm + C::OFF_K + s * C::KV_BYTES + c * C::CHUNK, &tm_k, &bars.kv_full[s],
-                      c * 64, hk, j * 128, b);
-          tma_load_4d(sm + C::OFF_V + s * C::KV_BYTES + c * C::CHUNK, &tm_v, &bars.kv_full[s],
-                      c * 64, hk, j * 128, b);
-        }
+        if (j >= 1) ok = load_v(j - 1);   // V stays one key tile behind K
       }
+      if (!ok) fail();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t sQ = saddr(sm + C::OFF_Q), sK = saddr(sm + C::OFF_K);
-      const uint32_t sV = saddr(sm + C::OFF_V), sP = saddr(sm + C::OFF_P);
-      bool ok = mbar_wait(&bars.q, 0);
-      auto pv = [&](int jj) -> bool {   // O += P_jj V_jj
-        const int s = jj & 1;
-        if (!mbar_wait(&bars.p_ready[s], (jj >> 1) & 1)) return false;
-        fence_after_sync();
-        const uint32_t pbase = sP + s * C::P_BYTES, vbase = sV + s * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::T_O, sdesc_sw128(pbase + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(vbase + kk * 2048, C::CHUNK, 1024), C::ID_O,
-                 (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.kv_empty[s]);
-        mma_commit(&bars.p_free[s]);
-        mma_commit(&bars.o_step);
-        return true;
-      };
-      for (int j = 0; ok && j < Tc; ++j) {
-        const int s = j & 1;
-        ok = !failed(&s_fail) && mbar_wait(&bars.kv_full[s], (j >> 1) & 1);
-        // S buffer s was last read by the softmax of tile j-2
-        if (ok && j >= 2) ok = mbar_wait(&bars.p_ready[s], ((j - 2) >> 1) & 1);
-        if (!ok) break;
-        fence_after_sync();
-        const uint32_t kbase = sK + s * C::KV_BYTES;
+      const uint32_t sV = saddr(sm + C::OFF_V);
+      auto issue_s = [&](int t, int j) {   // S_t(j) = Q_t K_j^T into S_t
+        const uint32_t qb = sQ + t * C::TILE_BYTES, kb = sK + (j % C::NK) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          mma_ss(tmem + C::T_S + s * 128, sdesc_sw128(sQ + off, 16, 1024),
-                 sdesc_sw128(kbase + off, 16, 1024), C::ID_S, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::T_S + t * 128, sdesc_sw128(qb + off, 16, 1024),
+                 sdesc_sw128(kb + off, 16, 1024), C::ID_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars.s_full[s]);
-        if (j >= 1) ok = pv(j - 1);
+        mma_commit(&bars.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) {  // O_t += P_t(j) V_j, P_t read from TMEM
+        const uint32_t vb = sV + (j % C::NV) * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::T_O + t * D, tmem + C::T_S + t * 128 + kk * 8,
+                 sdesc_sw128(vb + kk * 2048, C::CHUNK, 1024), C::ID_O,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&bars.q, 0) && mbar_wait(&bars.k_full[0], 0);
+      if (ok) {
+        fence_after_sync();
+        for (int t = 0; t < ntile; ++t) issue_s(t, 0);
+        mma_commit(&bars.k_empty[0]);
       }
-      if (ok && Tc >= 1) ok = pv(Tc - 1);
+      for (int j = 0; ok && j < Tc; ++j) {
+        const bool more = j + 1 < Tc;
+        if (more)
+          ok = !failed(&s_fail) &&
+               mbar_wait(&bars.k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1);
+        if (ok) ok = mbar_wait(&bars.v_full[j % C::NV], (j / C::NV) & 1);
+        for (int t = 0; ok && t < ntile; ++t) {
+          ok = mbar_wait(&bars.p_ready[t], j & 1);
+          if (!ok) break;
+          fence_after_sync();
+          issue_pv(t, j);
+          // S_t(j+1) overwrites P_t(j) in TMEM; it is queued after PV_t(j)
+          if (more) issue_s(t, j + 1);
+        }
+        if (!ok) break;
+        mma_commit(&bars.v_empty[j % C::NV]);
+        if (more) mma_commit(&bars.k_empty[(j + 1) % C::NK]);
+      }
       if (!ok) fail();
-      mma_commit(&bars.o_done);
+      for (int t = 0; t < 2; ++t) mma_commit(&bars.o_done[t]);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;                 // tile A (warps 4-7) or B (8-11)
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
-    const int row = qt * 128 + r;
+    const int row = (2 * pair + t) * 128 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t s_col = lane_base + C::T_S + t * 128;
+    const uint32_t o_col = lane_base + C::T_O + t * D;
     const int64_t bh = (int64_t)b * sh.H + h;
+    const bool valid_tile = t < ntile;
     float* st_row = stats ? stats + bh * sh.T_c * sh.n_pad + row : nullptr;
     float m_ref = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < Tc; ++j) {
-      const int s = j & 1;
-      ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.s_full[s], (j >> 1) & 1));
+    bool ok = valid_tile;
+    for (int j = 0; ok && j < Tc; ++j) {
+      ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.s_full[t], j & 1));
       if (!ok) break;
       fence_after_sync();
       uint32_t x[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t (&xc)[32] = *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]);
-        tmem_ld32(lane_base + C::T_S + s * 128 + c * 32, xc);
-      }
+      for (int c = 0; c < 4; ++c)
+        tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
       tmem_ld_wait();
-      const int valid = min(128, sh.n - j * 128);   // keys of this tile that exist
-      float mt = -INFINITY;
+      const int valid = sh.n - j * 128;            // keys of this tile that exist
+      if (valid < 128) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        float v = __uint_as_float(x[c]) * scale_log2;
-        v = c < valid ? v : -INFINITY;
-        x[c] = __float_as_uint(v);
-        mt = fmaxf(mt, v);
+        for (int c = 0; c < 128; ++c)
+          if (c >= valid) x[c] = __float_as_uint(-INFINITY);
       }
+      // max over the raw scores (the scale is positive), in base-2 units
+      float mr = __uint_as_float(x[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mr = fmaxf(mr, __uint_as_float(x[c]));
+      const float mt = mr * scale_log2;
       const bool grow = mt > m_ref + C::kRescale;
       const float m_new = grow ? mt : m_ref;
       const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
-      // P (bf16) into shared memory once the buffer's previous PV product is done
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.p_free[s], ((j >> 1) & 1) ^ 1));
-      if (!ok) break;
-      uint8_t* prow = sm + C::OFF_P + s * C::P_BYTES + r * 128;
       float ts = 0.f;
+      // p = 2^(x s log2 e - m); bf16 pairs packed in place (entry c from 2c, 2c+1)
 #pragma unroll
-      for (int k8 = 0; k8 < 16; ++k8) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(__uint_as_float(x[k8 * 8 + 2 * e]) - m_new);
-          const float p1 = fast_exp2(__uint_as_float(x[k8 * 8 + 2 * e + 1]) - m_new);
-          ts += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
-        }
-        const int chunk = k8 >> 3, piece = k8 & 7;
-        *reinterpret_cast<uint4*>(prow + chunk * C::CHUNK + ((piece ^ (r & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), scale_log2, -m_new));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), scale_log2, -m_new));
+        ts += p0 + p1;
+        x[c] = pack_bf16(p0, p1);
       }
-      if (st_row) st_row[(int64_t)j * sh.n_pad] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_st16(s_col + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&x[c * 16]));
+      if (st_row)
+        st_row[(int64_t)j * sh.n_pad] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
       l_run = l_run * alpha + ts;
       m_ref = m_new;
-      // rescale O in TMEM (rare): PV_{j-1} must have landed first
+      // rescale O in TMEM (rare).  S_t(j) has completed, hence so has PV_t(j-1):
+      // the MMA issuer queues S_t(j) behind it; PV_t(j) waits for p_ready.
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_step, (j - 1) & 1));
-        if (!ok) break;
-        fence_after_sync();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
           uint32_t ov[16];
-          tmem_ld16(lane_base + C::T_O + c0, ov);
+          tmem_ld16(o_col + c0, ov);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st16(lane_base + C::T_O + c0, ov);
+          tmem_st16(o_col + c0, ov);
         }
-        tmem_st_wait();
       }
-      fence_async_smem();
+      tmem_st_wait();
       fence_before_sync();
-      mbar_arrive(&bars.p_ready[s]);
+      mbar_arrive(&bars.p_ready[t]);
     }
-    if (!ok && lane == 0) fail();
-    // epilogue: O = acc / l, LSE = ln 2 (m + log2 l), once the last PV product landed
-    const bool done = __all_sync(0xffffffffu, ok && mbar_wait(&bars.o_done, 0));
-    fence_after_sync();
-    const float inv = 1.f / l_run;
-    __nv_bfloat16* orow = o + (((int64_t)b * sh.n + row) * sh.H + h) * D;
+    if (valid_tile) {
+      if (!ok && lane == 0) fail();
+      // epilogue: O = acc / l, LSE = ln 2 (m + log2 l), once the last PV landed
+      const bool done = __all_sync(0xffffffffu, ok && mbar_wait(&bars.o_done[t], 0));
+      fence_after_sync();
+      const float inv = 1.f / l_run;
+      __nv_bfloat16* orow = o + (((int64_t)b * sh.n + row) * sh.H + h) * D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t ov[32];
-      if (done) {
-        tmem_ld32(lane_base + C::T_O + c0, ov);
-        tmem_ld_wait();
-      }
-      if (done && row < sh.n) {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t ov[32];
+        if (done) {
+          tmem_ld32(o_col + c0, ov);
+          tmem_ld_wait();
+        }
+        if (done && row < sh.n) {
 #pragma unroll
-        for (int x8 = 0; x8 < 32; x8 += 8) {
-          uint4 w = make_uint4(
-              pack_bf16(__uint_as_float(ov[x8]) * inv, __uint_as_float(ov[x8 + 1]) * inv),
-              pack_bf16(__uint_as_float(ov[x8 + 2]) * inv, __uint_as_float(ov[x8 + 3]) * inv),
-              pack_bf16(__uint_as_float(ov[x8 + 4]) * inv, __uint_as_float(ov[x8 + 5]) * inv),
-              pack_bf16(__uint_as_float(ov[x8 + 6]) * inv, __uint_as_float(ov[x8 + 7]) * inv));
-          *reinterpret_cast<uint4*>(orow + c0 + x8) = w;
+          for (int x8 = 0; x8 < 32; x8 += 8) {
+            uint4 w = make_uint4(
+                pack_bf16(__uint_as_float(ov[x8]) * inv, __uint_as_float(ov[x8 + 1]) * inv),
+                pack_bf16(__uint_as_float(ov[x8 + 2]) * inv, __uint_as_float(ov[x8 + 3]) * inv),
+                pack_bf16(__uint_as_float(ov[x8 + 4]) * inv, __uint_as_float(ov[x8 + 5]) * inv),
+                pack_bf16(__uint_as_float(ov[x8 + 6]) * inv, __uint_as_float(ov[x8 + 7]) * inv));
+            *reinterpret_cast<uint4*>(orow + c0 + x8) = w;
+          }
         }
       }
+      // a forward that gave up on a bounded wait marks its rows' LSE with NaN
+      if (row < sh.n)
+        lse[bh * sh.n + row] =
+            done ? (m_ref + __log2f(l_run)) * kLn2 : __uint_as_float(0x7fc00000u);
+      if (!done && lane == 0) fail();
     }
-    // a forward that gave up on a bounded wait marks its rows' LSE with NaN
-    if (row < sh.n)
-      lse[bh * sh.n + row] = done ? (m_ref + __log2f(l_run)) * kLn2 : __uint_as_float(0x7fc00000u);
-    if (!done && lane == 0) fail();
   }
 
   fence_before_sync();
@@ -279,7 +299,7 @@ __global__ void __launch_bounds__(256, 1) fwd_tc_kernel(
 
 template <int D>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, void* o,
-                     float* lse, float* stats, int32_t* status, float scale, cudaStream_t st) {
+                     float* lse, float* stats, float scale, cudaStream_t st) {
   using C = FCfg<D>;
   CUtensorMap mq, mk, mv;
   if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
@@ -290,9 +310,8 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   auto kern = fwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(sh.T_r, sh.H, sh.B);
-  kern<<<grid, 256, smem, st>>>(mq, mk, mv, (__nv_bfloat16*)o, lse, stats, status, sh,
-                                scale * kLog2e);
+  dim3 grid((sh.T_r + 1) / 2, sh.H, sh.B);
+  kern<<<grid, 384, smem, st>>>(mq, mk, mv, (__nv_bfloat16*)o, lse, stats, sh, scale * kLog2e);
   return cudaGetLastError();
 }
 
@@ -305,8 +324,9 @@ bool fwd_tc_supported(const Shape& sh) {
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                           float* lse, float* stats, int32_t* status, float scale,
                           cudaStream_t st) {
-  if (sh.d == 128) return launch_t<128>(sh, q, k, v, o, lse, stats, status, scale, st);
-  return launch_t<64>(sh, q, k, v, o, lse, stats, status, scale, st);
+  (void)status;
+  if (sh.d == 128) return launch_t<128>(sh, q, k, v, o, lse, stats, scale, st);
+  return launch_t<64>(sh, q, k, v, o, lse, stats, scale, st);
 }
 
 }  // namespace bl
