@@ -10,27 +10,35 @@
 // softmax scale s at the end.  Skipped tiles are never loaded.
 //
 // One CTA per (key tile j, kv head, batch) walks, for each query head of its
-// GQA group, the ascending list of query tiles the mask keeps for j.  Each
-// query tile is handled as two halves of 64 rows so that every accumulator
-// fits the 512 TMEM columns of the SM:
-//   [0,64) S^T half   [64,128) dP^T half   [128,128+d) dQ (one query tile)
-//   [128+d,128+2d) dV   [128+2d,128+3d) dK
-// Warp roles (12 warps):
-//   warp 0      TMA producer: K_j, V_j once; then per half Q and dO (4-D
-//               tensor maps, 128-byte swizzle, out-of-range rows read as 0)
-//               into a 2-slot ring, plus the half's LSE and D rows.
-//   warp 1      MMA issuer (one thread) and TMEM owner.  Per half h it issues
-//               S^T_h, dP^T_h, then the gradient MMAs of half h-1 (dV, dK and,
-//               after the second half of a tile, dQ), so the softmax of h
-//               overlaps the tensor-core work of h-1.
-//   warps 4-7   softmax warpgroup: thread = key row; reads S^T/dP^T rows from
-//               TMEM, writes P^T and dS^T (bf16, swizzled) to shared memory;
-//               at the end writes dK, dV.
+// GQA group, the ascending list of query tiles the mask keeps for j.  Every
+// product is a 128 x 128 (x d) tcgen05.mma, the shape whose instructions keep
+// the tensor core busiest for M = 128.  TMEM (512 columns):
+//   R_S  [0,128)        S^T; after the softmax, P^T (bf16 pairs) in its
+//                       columns [0,32) and [64,96), read as the TMEM A operand
+//                       of dV += P^T dO
+//   R_dP [128,256)      dP^T; after the softmax, the dQ tile dS K
+//   dV   [256,256+d)    dK [256+d,256+2d)
+// The order in which one thread issues the MMAs makes every reuse safe: the
+// tensor core runs them in issue order, so S^T of the next tile (into R_S) is
+// queued behind dV (which reads P^T from R_S) and dQ (which reads dS^T from
+// shared memory), and dP^T of the next tile is issued only after the dQ
+// tile has been drained from R_dP.
+// Warp roles (16 warps):
+//   warp 0      TMA producer: K_j, V_j once; then Q_i and dO_i tiles into a
+//               3-slot ring (4-D tensor maps, 128-byte swizzle, rows past n
+//               read as 0), plus the tile's LSE and D rows.
+//   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2-3   at start: copy this CTA's tile lists into shared memory.
-//   warps 8-11  dQ warpgroup: thread = query row; drains the dQ tile from
-//               TMEM through a 128-byte-swizzled staging buffer (32 columns at
-//               a time) into the fp32 accumulator with TMA bulk reduce-adds,
-//               which the L2 applies as whole-line reductions.
+//   warps 4-7   softmax, query columns 0-63; warps 8-11 columns 64-127.
+//               Thread = key row: S^T, dP^T rows from TMEM -> P^T (TMEM) and
+//               dS^T (bf16, swizzled shared memory); at the end they write dV
+//               (warps 4-7) and dK (warps 8-11).
+//   warps 12-15 dQ drain: thread = query row; the dQ tile goes from TMEM
+//               through a 128-byte-swizzled staging buffer into the fp32
+//               accumulator with TMA bulk reduce-adds (whole-line L2 adds).
+// Registers: the block starts at 128 per thread; warps 0-3 give some back
+// (setmaxnreg.dec to 64) so the drain warpgroup can hold a whole 128-column
+// dQ row (setmaxnreg.inc to 192): 128*64 + 256*128 + 128*192 = 65536.
 // All hand-offs are mbarriers; every wait is bounded (tc.cuh).
 #include "common.cuh"
 #include "kernels.h"
@@ -44,38 +52,34 @@ using namespace tc;
 
 template <int D>
 struct Cfg {
-  static constexpr int BK = 128, HQ = 64, NS = 2;
+  static constexpr int NS = 3;                    // ring slots, one Q or dO tile each
   static constexpr int CHK = D / 64;              // 64-element chunks along d
-  static constexpr int KV_CHUNK = BK * 128;       // [128 rows][128 B]
-  static constexpr int QH_CHUNK = HQ * 128;       // [64 rows][128 B]
-  static constexpr int KV_BYTES = KV_CHUNK * CHK;
-  static constexpr int QH_BYTES = QH_CHUNK * CHK;
-  static constexpr int P_BYTES = BK * HQ * 2;     // [128 keys][64 q] bf16
+  static constexpr int CHUNK = 128 * 128;         // [128 rows][128 B]
+  static constexpr int TILE = CHUNK * CHK;        // one 128 x d bf16 tile
+  static constexpr int DS_BYTES = 2 * CHUNK;      // dS^T [128 keys][128 q] bf16
   static constexpr int STAGE_BYTES = 128 * 128;   // dQ staging: [128 rows][32 fp32]
   static constexpr int LIST_CAP = 2048;           // cached list entries per CTA
   static constexpr int GMAX = 32;                 // heads per GQA group with cached lists
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;
-  static constexpr int OFF_G = OFF_Q + NS * QH_BYTES;
-  static constexpr int OFF_P = OFF_G + NS * QH_BYTES;
-  static constexpr int OFF_S = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_STAGE = OFF_S + 2 * P_BYTES;
-  static constexpr int OFF_L = OFF_STAGE + STAGE_BYTES;   // NS x 64 floats: lse*log2e
-  static constexpr int OFF_D = OFF_L + NS * HQ * 4;       // NS x 64 floats: D
-  static constexpr int OFF_LIST = OFF_D + NS * HQ * 4;    // LIST_CAP ints
-  static constexpr int OFF_LCNT = OFF_LIST + LIST_CAP * 4;  // GMAX ints
-  static constexpr int OFF_LBASE = OFF_LCNT + GMAX * 4;     // GMAX ints
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_RING = OFF_V + TILE;
+  static constexpr int OFF_DS = OFF_RING + NS * TILE;
+  static constexpr int OFF_STAGE = OFF_DS + DS_BYTES;
+  static constexpr int OFF_L = OFF_STAGE + STAGE_BYTES;   // NS x 128 floats: lse*log2e
+  static constexpr int OFF_D = OFF_L + NS * 128 * 4;      // NS x 128 floats: D
+  static constexpr int OFF_LIST = OFF_D + NS * 128 * 4;   // LIST_CAP ints
+  static constexpr int OFF_LCNT = OFF_LIST + LIST_CAP * 4;
+  static constexpr int OFF_LBASE = OFF_LCNT + GMAX * 4;
   static constexpr int BYTES = OFF_LBASE + GMAX * 4;
-  static constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 128 + D, T_DK = 128 + 2 * D;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DV = 256, T_DK = 256 + D;
   static constexpr uint32_t T_COLS = 512;
-  static constexpr uint32_t ID_S = idesc_bf16(128, 64, false, false);
-  static constexpr uint32_t ID_G = idesc_bf16(128, D, false, true);
-  static constexpr uint32_t ID_Q = idesc_bf16(128, D, true, true);
+  static constexpr uint32_t ID_SS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+  static constexpr uint32_t ID_G = idesc_bf16(128, D, false, true);      // dV, dK
+  static constexpr uint32_t ID_Q = idesc_bf16(128, D, true, true);       // dQ
 };
 
 struct Bars {
-  uint64_t kv, full[2], empty[2], s, p, pfree[2], dsfree, dqready, dqfree, acc;
+  uint64_t kv, full[3], empty[3], s_full, dp_full, p_ready, dq_ready, dq_free, acc;
 };
 
 // Iterates the kept query tiles of key tile j over the heads of one GQA group,
@@ -131,13 +135,14 @@ struct Walk {
 __device__ __forceinline__ bool failed(const int* f) { return *(volatile const int*)f != 0; }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
+__global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse, const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
+    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+    const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
     const int32_t* __restrict__ q_cnt, __nv_bfloat16* __restrict__ g_k,
-    __nv_bfloat16* __restrict__ g_v, float* __restrict__ dq_acc, int32_t* __restrict__ status,
-    Shape sh, float scale, float scale_log2) {
+    __nv_bfloat16* __restrict__ g_v, int32_t* __restrict__ status, Shape sh, float scale,
+    float scale_log2) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -154,16 +159,14 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv, 1);
     for (int s = 0; s < C::NS; ++s) {
-      mbar_init(&bars.full[s], 33);
+      mbar_init(&bars.full[s], 33);   // 32 producer lanes + the expect_tx arrival
       mbar_init(&bars.empty[s], 1);
     }
-    mbar_init(&bars.s, 1);
-    mbar_init(&bars.p, 128);
-    mbar_init(&bars.pfree[0], 1);
-    mbar_init(&bars.pfree[1], 1);
-    mbar_init(&bars.dsfree, 1);
-    mbar_init(&bars.dqready, 1);
-    mbar_init(&bars.dqfree, 128);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.p_ready, 256);
+    mbar_init(&bars.dq_ready, 1);
+    mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.acc, 1);
     s_fail = 0;
     fence_mbar_init();
@@ -216,229 +219,248 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
   };
   const bool cached = s_cached != 0;
   Walk walk{q_idx, q_cnt, &sh, j, b, hk, G, cached ? s_list : nullptr, s_lcnt, s_lbase};
-
-  if (warp == 0) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
       prefetch_tmap(&tm_g);
-      mbar_expect_tx(&bars.kv, 2 * C::KV_BYTES);
+      mbar_expect_tx(&bars.kv, 2 * C::TILE);
       for (int c = 0; c < C::CHK; ++c) {
-        tma_load_4d(sm + C::OFF_K + c * C::KV_CHUNK, &tm_k, &bars.kv, c * 64, hk, j * 128, b);
-        tma_load_4d(sm + C::OFF_V + c * C::KV_CHUNK, &tm_v, &bars.kv, c * 64, hk, j * 128, b);
+        tma_load_4d(sm + C::OFF_K + c * C::CHUNK, &tm_k, &bars.kv, c * 64, hk, j * 128, b);
+        tma_load_4d(sm + C::OFF_V + c * C::CHUNK, &tm_v, &bars.kv, c * 64, hk, j * 128, b);
       }
     }
-    int hc = 0;
-    while (walk.next()) {
+    int x = 0;   // load index: 2t for Q of tile t, 2t+1 for its dO
+    bool ok = true;
+    while (ok && walk.next()) {
       const int64_t bh = (int64_t)b * sh.H + walk.h;
-      for (int half = 0; half < 2; ++half, ++hc) {
-        const int s = hc % C::NS;
-        const int r0 = walk.i * 128 + half * 64;
-        // start the LSE and D loads of this half before waiting for its slot
-        float lv[2], dv[2];
+      const int r0 = walk.i * 128;
+      for (int which = 0; which < 2 && ok; ++which, ++x) {
+        const int s = x % C::NS;
+        float lv[4], dv[4];
+        if (which == 0) {   // this tile's LSE and D travel with its Q slot
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int r = r0 + lane + 32 * e;
-          const bool ok = r < sh.n;
-          lv[e] = ok ? lse[bh * sh.n + r] * kLog2e : INFINITY;
-          dv[e] = ok ? Dv[bh * sh.n + r] : 0.f;
-        }
-        if (failed(&s_fail) || !mbar_wait(&bars.empty[s], ((hc / C::NS) & 1) ^ 1)) {
-          if (lane == 0) fail();
-          goto producer_done;
-        }
-        if (lane == 0) {
-          mbar_expect_tx(&bars.full[s], 2 * C::QH_BYTES);
-          for (int c = 0; c < C::CHK; ++c) {
-            tma_load_4d(sm + C::OFF_Q + s * C::QH_BYTES + c * C::QH_CHUNK, &tm_q, &bars.full[s],
-                        c * 64, walk.h, r0, b);
-            tma_load_4d(sm + C::OFF_G + s * C::QH_BYTES + c * C::QH_CHUNK, &tm_g, &bars.full[s],
-                        c * 64, walk.h, r0, b);
+          for (int e = 0; e < 4; ++e) {
+            const int r = r0 + lane + 32 * e;
+            const bool in = r < sh.n;
+            lv[e] = in ? lse[bh * sh.n + r] * kLog2e : INFINITY;
+            dv[e] = in ? Dv[bh * sh.n + r] : 0.f;
           }
         }
-        float* sl = reinterpret_cast<float*>(sm + C::OFF_L) + s * 64;
-        float* sd = reinterpret_cast<float*>(sm + C::OFF_D) + s * 64;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          sl[lane + 32 * e] = lv[e];
-          sd[lane + 32 * e] = dv[e];
+        ok = !failed(&s_fail) && mbar_wait(&bars.empty[s], ((x / C::NS) & 1) ^ 1);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_expect_tx(&bars.full[s], C::TILE);
+          for (int c = 0; c < C::CHK; ++c)
+            tma_load_4d(sm + C::OFF_RING + s * C::TILE + c * C::CHUNK, which ? &tm_g : &tm_q,
+                        &bars.full[s], c * 64, walk.h, r0, b);
         }
-        mbar_arrive(&bars.full[s]);   // with lane 0's expect_tx arrival: 33 per phase
+        if (which == 0) {
+          float* sl = reinterpret_cast<float*>(sm + C::OFF_L) + s * 128;
+          float* sd = reinterpret_cast<float*>(sm + C::OFF_D) + s * 128;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sl[lane + 32 * e] = lv[e];
+            sd[lane + 32 * e] = dv[e];
+          }
+        }
+        mbar_arrive(&bars.full[s]);
       }
     }
+    if (!ok && lane == 0) fail();
     if (lane == 0 && walk.corrupt) atomicOr(status, kStatusCorrupt);
-  producer_done:;
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t sK = saddr(sm + C::OFF_K), sV = saddr(sm + C::OFF_V);
-      const uint32_t sQ = saddr(sm + C::OFF_Q), sG = saddr(sm + C::OFF_G);
-      const uint32_t sP = saddr(sm + C::OFF_P), sS = saddr(sm + C::OFF_S);
-      bool ok = mbar_wait(&bars.kv, 0);
-      int hc = 0;
-      // gradient MMAs of half g (slot g % NS, P/dS buffer g % 2)
-      auto grads = [&](int g) -> bool {
-        const int slot = g % C::NS, pb = g & 1;
-        const uint32_t q_half = sQ + slot * C::QH_BYTES, g_half = sG + slot * C::QH_BYTES;
+      const uint32_t sR = saddr(sm + C::OFF_RING), sDS = saddr(sm + C::OFF_DS);
+      auto slot_addr = [&](int xx) { return sR + (xx % C::NS) * C::TILE; };
+      auto issue_s = [&](int t) {      // S^T = K Q_t^T  -> R_S
+        const uint32_t qb = slot_addr(2 * t);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (g > 0 || kk > 0) ? 1u : 0u;
-          mma_ss(tmem + C::T_DV, sdesc_sw128(sP + pb * C::P_BYTES + kk * 32, 16, 1024),
-                 sdesc_sw128(g_half + kk * 2048, C::QH_CHUNK, 1024), C::ID_G, acc);
-          mma_ss(tmem + C::T_DK, sdesc_sw128(sS + pb * C::P_BYTES + kk * 32, 16, 1024),
-                 sdesc_sw128(q_half + kk * 2048, C::QH_CHUNK, 1024), C::ID_G, acc);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+          mma_ss(tmem + C::T_S, sdesc_sw128(sK + off, 16, 1024),
+                 sdesc_sw128(qb + off, 16, 1024), C::ID_SS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars.pfree[pb]);
-        mma_commit(&bars.empty[slot]);
-        if (pb == 1) {
-          const int u = g >> 1;
-          if (!mbar_wait(&bars.dqfree, (u & 1) ^ 1)) return false;
-          fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::T_DQ, sdesc_sw128(sS + kk * 2048, C::P_BYTES, 1024),
-                   sdesc_sw128(sK + kk * 2048, C::KV_CHUNK, 1024), C::ID_Q, kk > 0 ? 1u : 0u);
-          mma_commit(&bars.dqready);
-          mma_commit(&bars.dsfree);
-        }
-        return true;
+        mma_commit(&bars.s_full);
       };
-      while (ok && walk.next()) {
-        for (int half = 0; half < 2 && ok; ++half, ++hc) {
-          const int s = hc % C::NS;
-          ok = !failed(&s_fail) && mbar_wait(&bars.full[s], (hc / C::NS) & 1);
-          if (ok && hc > 0) ok = mbar_wait(&bars.p, (hc - 1) & 1);
-          if (!ok) break;
-          fence_after_sync();
-          const uint32_t q_half = sQ + s * C::QH_BYTES, g_half = sG + s * C::QH_BYTES;
+      auto issue_dp = [&](int t) {     // dP^T = V dO_t^T -> R_dP
+        const uint32_t gb = slot_addr(2 * t + 1);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * C::QH_CHUNK + (kk & 3) * 32;
-            mma_ss(tmem + C::T_S, sdesc_sw128(sK + ko, 16, 1024),
-                   sdesc_sw128(q_half + qo, 16, 1024), C::ID_S, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * C::QH_CHUNK + (kk & 3) * 32;
-            mma_ss(tmem + C::T_DP, sdesc_sw128(sV + ko, 16, 1024),
-                   sdesc_sw128(g_half + qo, 16, 1024), C::ID_S, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars.s);
-          if (hc > 0) ok = grads(hc - 1);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+          mma_ss(tmem + C::T_DP, sdesc_sw128(sV + off, 16, 1024),
+                 sdesc_sw128(gb + off, 16, 1024), C::ID_SS, kk > 0 ? 1u : 0u);
         }
-      }
-      if (ok && hc > 0) {
-        ok = mbar_wait(&bars.p, (hc - 1) & 1);
+        mma_commit(&bars.dp_full);
+      };
+      auto wait_slot = [&](int xx) {
+        return mbar_wait(&bars.full[xx % C::NS], (xx / C::NS) & 1);
+      };
+      bool ok = mbar_wait(&bars.kv, 0);
+      int t = 0;
+      bool have = ok && walk.next();
+      if (have) {
+        ok = wait_slot(0);
         if (ok) {
           fence_after_sync();
-          ok = grads(hc - 1);
+          issue_s(0);
+          ok = wait_slot(1);
+          if (ok) {
+            fence_after_sync();
+            issue_dp(0);
+          }
         }
+      }
+      while (ok && have) {
+        // gradients of tile t once its softmax has written P^T and dS^T
+        ok = !failed(&s_fail) && mbar_wait(&bars.p_ready, t & 1);
+        if (!ok) break;
+        fence_after_sync();
+        const uint32_t qb = slot_addr(2 * t), gb = slot_addr(2 * t + 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {      // dV += P^T dO  (P^T from TMEM)
+          const uint32_t pcol = C::T_S + (kk >> 2) * 64 + (kk & 3) * 8;
+          mma_ts(tmem + C::T_DV, tmem + pcol, sdesc_sw128(gb + kk * 2048, C::CHUNK, 1024),
+                 C::ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)        // dK += dS^T Q
+          mma_ss(tmem + C::T_DK,
+                 sdesc_sw128(sDS + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(qb + kk * 2048, C::CHUNK, 1024), C::ID_G,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.empty[(2 * t) % C::NS]);
+        mma_commit(&bars.empty[(2 * t + 1) % C::NS]);
+        // dQ = dS K into R_dP (dP^T was consumed by the softmax)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::T_DP, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024),
+                 sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024), C::ID_Q, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.dq_ready);
+        have = walk.next();
+        if (have) {
+          ok = wait_slot(2 * (t + 1));
+          if (!ok) break;
+          fence_after_sync();
+          issue_s(t + 1);                     // queued behind dV and dQ of tile t
+          ok = mbar_wait(&bars.dq_free, t & 1) && wait_slot(2 * (t + 1) + 1);
+          if (!ok) break;
+          fence_after_sync();
+          issue_dp(t + 1);
+        }
+        ++t;
       }
       if (!ok) fail();
       mma_commit(&bars.acc);
     }
-  } else if (warp >= 4 && warp < 8) {
+   }
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
+    const int half = (warp - 4) >> 2;           // query columns [64 half, 64 half + 64)
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;                  // key row within the tile
+    const int r = q4 * 32 + lane;               // key row within the tile
     const bool key_ok = j * 128 + r < sh.n;
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint8_t* sP = sm + C::OFF_P;
-    uint8_t* sS = sm + C::OFF_S;
-    int hc = 0;
+    uint8_t* ds_row = sm + C::OFF_DS + half * C::CHUNK + r * 128;
+    int t = 0;
     bool ok = true;
     while (ok && walk.next()) {
-      for (int half = 0; half < 2; ++half, ++hc) {
-        const int s = hc % C::NS, pb = hc & 1, u = hc >> 1;
-        ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
-                                         mbar_wait(&bars.full[s], (hc / C::NS) & 1) &&
-                                         mbar_wait(&bars.s, hc & 1));
-        if (!ok) break;
-        fence_after_sync();
-        uint32_t sv[2][32], pv[2][32];
-        tmem_ld32(lane_base + C::T_S, sv[0]);
-        tmem_ld32(lane_base + C::T_S + 32, sv[1]);
-        tmem_ld32(lane_base + C::T_DP, pv[0]);
-        tmem_ld32(lane_base + C::T_DP + 32, pv[1]);
+      const int s = (2 * t) % C::NS;
+      ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
+                                       mbar_wait(&bars.full[s], ((2 * t) / C::NS) & 1) &&
+                                       mbar_wait(&bars.s_full, t & 1) &&
+                                       mbar_wait(&bars.dp_full, t & 1));
+      if (!ok) break;
+      fence_after_sync();
+      const float* sl = reinterpret_cast<const float*>(sm + C::OFF_L) + s * 128 + half * 64;
+      const float* sd = reinterpret_cast<const float*>(sm + C::OFF_D) + s * 128 + half * 64;
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {    // 32 query columns per pass
+        const int cb = half * 64 + pass * 32;
+        uint32_t sv[32], pv[32];
+        tmem_ld32(lane_base + C::T_S + cb, sv);
+        tmem_ld32(lane_base + C::T_DP + cb, pv);
         tmem_ld_wait();
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.pfree[pb], ((hc >> 1) & 1) ^ 1) &&
-                                         mbar_wait(&bars.dsfree, (u & 1) ^ 1));
-        if (!ok) break;
-        const float* sl = reinterpret_cast<const float*>(sm + C::OFF_L) + s * 64;
-        const float* sd = reinterpret_cast<const float*>(sm + C::OFF_D) + s * 64;
-        uint8_t* prow = sP + pb * C::P_BYTES + r * 128;
-        uint8_t* srow = sS + pb * C::P_BYTES + r * 128;
+        float lrow[32], drow[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {      // 8 columns (16 bytes) at a time
-          uint32_t pk[4], dk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float p2[2], d2[2];
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              const int c = c8 * 8 + e * 2 + x;
-              const float sc = __uint_as_float(sv[c >> 5][c & 31]);
-              const float dp = __uint_as_float(pv[c >> 5][c & 31]);
-              const float p = key_ok ? fast_exp2(fmaf(sc, scale_log2, -sl[c])) : 0.f;
-              p2[x] = p;
-              d2[x] = p * (dp - sd[c]);
-            }
-            pk[e] = pack_bf16(p2[0], p2[1]);
-            dk[e] = pack_bf16(d2[0], d2[1]);
-          }
-          const int phys = (c8 ^ (r & 7)) * 16;
-          *reinterpret_cast<uint4*>(prow + phys) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(srow + phys) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 a = reinterpret_cast<const float4*>(sl + pass * 32)[c4];
+          const float4 d4 = reinterpret_cast<const float4*>(sd + pass * 32)[c4];
+          lrow[4 * c4] = a.x; lrow[4 * c4 + 1] = a.y; lrow[4 * c4 + 2] = a.z; lrow[4 * c4 + 3] = a.w;
+          drow[4 * c4] = d4.x; drow[4 * c4 + 1] = d4.y; drow[4 * c4 + 2] = d4.z; drow[4 * c4 + 3] = d4.w;
         }
-        fence_async_smem();
-        fence_before_sync();
-        mbar_arrive(&bars.p);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float p2[2], d2[2];
+#pragma unroll
+          for (int y = 0; y < 2; ++y) {
+            const int c = 2 * e + y;
+            const float p =
+                key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lrow[c])) : 0.f;
+            p2[y] = p;
+            d2[y] = p * (__uint_as_float(pv[c]) - drow[c]);
+          }
+          pk[e] = pack_bf16(p2[0], p2[1]);
+          dk[e] = pack_bf16(d2[0], d2[1]);
+        }
+        // P^T pairs over this warpgroup's own S^T columns (already read)
+        tmem_st16(lane_base + C::T_S + half * 64 + pass * 16, pk);
+        // dS^T, K-major [key][q] with the 128-byte swizzle, 4 x 16 B chunks
+#pragma unroll
+        for (int c16 = 0; c16 < 4; ++c16) {
+          const int chunk = pass * 4 + c16;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
+        }
       }
+      tmem_st_wait();
+      fence_async_smem();
+      fence_before_sync();
+      mbar_arrive(&bars.p_ready);
+      ++t;
     }
     if (!ok && lane == 0) fail();
-    // epilogue: dV, dK rows of this key tile (accumulators complete at bars.acc)
+    // epilogue: warps 4-7 write dV, warps 8-11 dK (scaled), rows of this key tile
     const bool acc_ok = mbar_wait(&bars.acc, 0);
     fence_after_sync();
-    const bool have = __all_sync(0xffffffffu, ok && acc_ok) && hc > 0;
+    const bool have = __all_sync(0xffffffffu, ok && acc_ok) && t > 0;
     const int key = j * 128 + r;
-    __nv_bfloat16* vr = g_v + (((int64_t)b * sh.n + key) * sh.Hk + hk) * D;
-    __nv_bfloat16* kr = g_k + (((int64_t)b * sh.n + key) * sh.Hk + hk) * D;
+    __nv_bfloat16* dst = (half == 0 ? g_v : g_k) + (((int64_t)b * sh.n + key) * sh.Hk + hk) * D;
+    const float mul = half == 0 ? 1.f : scale;
+    const uint32_t col = half == 0 ? C::T_DV : C::T_DK;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t a[32], k2[32];
+      uint32_t a[32];
       if (have) {  // warp-uniform: the TMEM loads are warp-collective
-        tmem_ld32(lane_base + C::T_DV + c0, a);
-        tmem_ld32(lane_base + C::T_DK + c0, k2);
+        tmem_ld32(lane_base + col + c0, a);
         tmem_ld_wait();
       }
       if (key < sh.n) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 8) {
-          uint4 wv = make_uint4(0u, 0u, 0u, 0u), wk = make_uint4(0u, 0u, 0u, 0u);
-          if (have) {
-            wv = make_uint4(pack_bf16(__uint_as_float(a[x]), __uint_as_float(a[x + 1])),
-                            pack_bf16(__uint_as_float(a[x + 2]), __uint_as_float(a[x + 3])),
-                            pack_bf16(__uint_as_float(a[x + 4]), __uint_as_float(a[x + 5])),
-                            pack_bf16(__uint_as_float(a[x + 6]), __uint_as_float(a[x + 7])));
-            wk = make_uint4(
-                pack_bf16(__uint_as_float(k2[x]) * scale, __uint_as_float(k2[x + 1]) * scale),
-                pack_bf16(__uint_as_float(k2[x + 2]) * scale, __uint_as_float(k2[x + 3]) * scale),
-                pack_bf16(__uint_as_float(k2[x + 4]) * scale, __uint_as_float(k2[x + 5]) * scale),
-                pack_bf16(__uint_as_float(k2[x + 6]) * scale, __uint_as_float(k2[x + 7]) * scale));
-          }
-          *reinterpret_cast<uint4*>(vr + c0 + x) = wv;
-          *reinterpret_cast<uint4*>(kr + c0 + x) = wk;
+        for (int x8 = 0; x8 < 32; x8 += 8) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (have)
+            w = make_uint4(
+                pack_bf16(__uint_as_float(a[x8]) * mul, __uint_as_float(a[x8 + 1]) * mul),
+                pack_bf16(__uint_as_float(a[x8 + 2]) * mul, __uint_as_float(a[x8 + 3]) * mul),
+                pack_bf16(__uint_as_float(a[x8 + 4]) * mul, __uint_as_float(a[x8 + 5]) * mul),
+                pack_bf16(__uint_as_float(a[x8 + 6]) * mul, __uint_as_float(a[x8 + 7]) * mul));
+          *reinterpret_cast<uint4*>(dst + c0 + x8) = w;
         }
       }
     }
-  } else if (warp >= 8) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
     // ------------------------------------------------------------ dQ drain
     const int q4 = warp & 3;
-    const int dt = threadIdx.x - 256;              // 0..127, = row within the tile
+    const int dt = threadIdx.x - 384;              // 0..127, = query row within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     uint8_t* stage = sm + C::OFF_STAGE;
     uint8_t* srow = stage + dt * 128;
@@ -447,28 +469,28 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(
     while (ok && walk.next()) {
       // the four drain warps agree on success before any named barrier
       const bool w_ok =
-          __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.dqready, u & 1));
+          __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.dq_ready, u & 1));
       if (lane == 0) s_drain_ok[q4] = w_ok;
       named_sync(1, 128);
       ok = s_drain_ok[0] && s_drain_ok[1] && s_drain_ok[2] && s_drain_ok[3];
       named_sync(1, 128);
       if (!ok) break;
       fence_after_sync();
-#pragma unroll 1
+      uint32_t a[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32)
+        tmem_ld32(lane_base + C::T_DP + c0, *reinterpret_cast<uint32_t(*)[32]>(&a[c0]));
+      tmem_ld_wait();
+      fence_before_sync();
+      mbar_arrive(&bars.dq_free);    // R_dP is free for the next dP^T
+#pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t a[32];
-        tmem_ld32(lane_base + C::T_DQ + c0, a);
-        tmem_ld_wait();
-        if (c0 + 32 == D) {          // the dQ columns of TMEM are free again
-          fence_before_sync();
-          mbar_arrive(&bars.dqfree);
-        }
         if (dt == 0) bulk_wait_read0();   // previous reduce has read the staging rows
         named_sync(1, 128);
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
-          *reinterpret_cast<uint4*>(srow + ((x ^ (dt & 7)) << 4)) =
-              make_uint4(a[4 * x], a[4 * x + 1], a[4 * x + 2], a[4 * x + 3]);
+        for (int y = 0; y < 8; ++y)
+          *reinterpret_cast<uint4*>(srow + ((y ^ (dt & 7)) << 4)) =
+              make_uint4(a[c0 + 4 * y], a[c0 + 4 * y + 1], a[c0 + 4 * y + 2], a[c0 + 4 * y + 3]);
         fence_async_smem();
         named_sync(1, 128);
         if (dt == 0) {
@@ -494,8 +516,10 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
                      float scale, cudaStream_t st) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv, mg, md;
-  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 64) || !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 64) ||
-      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) || !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
+  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
+      !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 128) ||
+      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) ||
+      !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
       !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
@@ -503,8 +527,8 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(sh.T_c, sh.Hk, sh.B);
-  kern<<<grid, 384, smem, st>>>(mq, mk, mv, mg, md, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
-                                (__nv_bfloat16*)g_v, dq_acc, status, sh, scale, scale * kLog2e);
+  kern<<<grid, 512, smem, st>>>(mq, mk, mv, mg, md, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
+                                (__nv_bfloat16*)g_v, status, sh, scale, scale * kLog2e);
   return cudaGetLastError();
 }
 
