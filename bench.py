@@ -328,7 +328,10 @@ def run_ours(args):
     # counting only the valid rows/keys of ragged edge tiles
     computed_flop = _active_flop(mask, w)
     bwd_only = statistics.mean(bwd_ms)
+    fwd_only = statistics.mean(fwd_ms)
     achieved_tf = computed_flop / (bwd_only * 1e-3) / 1e12
+    fwd_tf = w.dense_fwd_flop() / (fwd_only * 1e-3) / 1e12
+    traffic = _traffic(args.workload)
     line = {
         "metric": METRIC, "value": attn_bwd_ms, "unit": "ms", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -343,10 +346,25 @@ def run_ours(args):
         "dense_equiv_tflops": dense_flop / (attn_bwd_ms * 1e-3) / 1e12,
         "skip_frac": skip,
         "frac_bf16_peak_computed_tiles": achieved_tf / pk["bf16"],
-        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16"],
-                     "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16"], "traffic": None,
-                     "kernel": "bl_attn_bwd (all its launches; dK/dV pass dominant)",
-                     "peak_src": pk["src"]},
+        # the step's dominant kernel (by time): the forward with tile statistics
+        "roofline": {"bound": "tensor", "achieved": fwd_tf, "peak": pk["bf16"],
+                     "unit": "TFLOP/s", "frac": fwd_tf / pk["bf16"],
+                     "traffic": traffic.get("fwd_tc_kernel"),
+                     "kernel": "fwd_tc_kernel (4*B*H*n^2*d per launch)",
+                     "peak_src": pk["src"] + " burst"},
+        # the metric's own kernel: the block-sparse backward on computed tiles
+        "roofline_bwd": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16"],
+                         "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16"],
+                         "traffic": traffic.get("bwd_tc_kernel"),
+                         "kernel": "bl_attn_bwd call (bwd_tc_kernel + D pass + dQ convert + "
+                                   "memset), 10*d*valid rows*valid keys per kept tile",
+                         "peak_src": pk["src"] + " burst"},
+        "roofline_mask": {"bound": "hbm",
+                          "achieved": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
+                          "peak": pk["hbm"], "unit": "GB/s",
+                          "frac": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9 / pk["hbm"],
+                          "traffic": traffic.get("mask_rows_kernel"),
+                          "kernel": "bl_mask_from_stats call (both kernels)"},
         "gpu_launches": 6 * args.steps,
     }
     clk_s = clk.summary()
@@ -364,6 +382,33 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _mask_bytes(w):
+    """Algorithmic bytes of bl_mask_from_stats: read the tile statistics and
+    the LSE, write mask, kv_idx, kv_cnt, q_idx, q_cnt."""
+    stats = w.B * w.H * w.T_c * w.T_r * w.block_q * 4
+    lse = w.B * w.H * w.n * 4
+    lists = w.B * w.H * w.T_r * w.T_c * (1 + 4 + 4) + w.B * w.H * (w.T_r + w.T_c) * 4
+    return stats + lse + lists
+
+
+def _traffic(workload):
+    """Per-launch DRAM bytes (read + write) of the kernels on this workload from
+    the committed ncu summary, for every kernel whose source is unchanged since
+    the counters were taken (same SHA-256 of its .cu file); else absent."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return {}
+    d = json.load(open(p))
+    out = {}
+    for kernel, rec in d.get(workload, {}).items():
+        src = os.path.join(ROOT, "block_sparse_attention_fwd_gb300", "csrc", rec["source"])
+        if os.path.exists(src) and \
+                hashlib.sha256(open(src, "rb").read()).hexdigest() == rec["sha256"]:
+            out[kernel] = rec["dram_bytes_per_launch"]
+    return out
 
 
 def _active_flop(mask, w):
@@ -422,6 +467,74 @@ def _e2e(args, w, shape, q, k, v, go, negl, dev):
             "d2h_bytes_per_step": d2h}
 
 
+def run_all_configs(args):
+    """One JSON line per workload (and negl_prob) with the per-kernel times;
+    these fill the per-configuration table, they are not the contract line."""
+    import torch
+
+    from block_sparse_attention_fwd_gb300 import _lib, build, inputs
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pk = _peaks()
+    for name in ("tiny_n256_d64", "clustered_n4096_d64", "gqa_n8192_d128",
+                 "video_n32760_d128", "long_n131072_d128"):
+        w = inputs.WORKLOADS[name]
+        q, k, v, go = inputs.generate(w, seed=0)
+        shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+        T_r, T_c = _lib.tiles(shape)
+        qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
+        o = torch.empty_like(qd)
+        lse = torch.empty((w.B, w.H, w.n), dtype=torch.float32, device=dev)
+        stats = torch.empty((w.B, w.H, T_c, T_r * w.block_q), dtype=torch.float32, device=dev)
+        lists = _lib.alloc_lists(shape, dev)
+        g_q, g_k, g_v = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+
+        def timed(fn, reps):
+            fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return statistics.median(ts)
+
+        reps = 3 if w.n >= 100000 else 5
+        fwd = timed(lambda: _lib.attn_fwd(shape, qd, kd, vd, w.scale, o, lse, stats), reps)
+        dense = timed(lambda: _lib.attn_bwd(shape, qd, kd, vd, o, god, lse, w.scale, None, g_q,
+                                            g_k, g_v, wsb), reps)
+        for negl in w.negl_probs:
+            mask_ms = timed(lambda: _lib.mask_from_stats(shape, stats, lse, negl, lists), reps)
+            bwd = timed(lambda: _lib.attn_bwd(shape, qd, kd, vd, o, god, lse, w.scale, lists, g_q,
+                                              g_k, g_v, wsb), reps)
+            mask = lists["mask"]
+            skip = 1.0 - float(mask.float().mean())
+            comp = _active_flop(mask, w)
+            line = {"workload": name, "negl_prob": negl, "fwd_ms": fwd,
+                    "fwd_tflops": w.dense_fwd_flop() / fwd / 1e9,
+                    "mask_ms": mask_ms, "mask_gbs": _mask_bytes(w) / mask_ms / 1e6,
+                    "bwd_ms": bwd, "attn_bwd_ms": mask_ms + bwd,
+                    "dense_equiv_tflops": w.dense_bwd_flop() / (mask_ms + bwd) / 1e9,
+                    "skip_frac": skip,
+                    "frac_bf16_peak_computed_tiles": comp / bwd / 1e9 / pk["bf16"],
+                    "dense_bwd_ms": dense,
+                    "dense_bwd_frac_peak": w.dense_bwd_flop() / dense / 1e9 / pk["bf16"]}
+            if not args.no_cpu_baseline:
+                ms_cpu, desc, tiles, el = cpu_reference_sample(w, q, k, v, go, budget_s=5.0,
+                                                               max_tiles=64)
+                line["oracle_bwd_ms_extrapolated"] = ms_cpu
+                line["oracle_sample"] = f"{tiles} query tiles in {el:.1f} s, {os.cpu_count()} cores"
+            print(json.dumps(line), flush=True)
+        del qd, kd, vd, god, o, lse, stats, lists, g_q, g_k, g_v, wsb
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -435,7 +548,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--ref-tiles", type=int, default=256)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="per-workload kernel times (not the contract line)")
     args = ap.parse_args()
+    if args.all_configs:
+        return run_all_configs(args)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

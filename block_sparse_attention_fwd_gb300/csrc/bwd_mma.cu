@@ -29,14 +29,26 @@ namespace {
 constexpr int QC = 64;  // query rows per chunk
 
 // D[b,h,r] = sum_d G_O[b,r,h,d] * O[b,r,h,d]: one warp per (b, r, h) row.
+// The same warp zeroes that row of the fp32 dQ accumulator, and block 0 the
+// status word, so no separate memset pass is needed.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ g_o,
-                                                      float* __restrict__ Dv, Shape sh) {
+                                                      float* __restrict__ Dv,
+                                                      float* __restrict__ dq_acc,
+                                                      int32_t* __restrict__ status, Shape sh) {
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t total = (int64_t)sh.B * sh.n * sh.H;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
   if (row >= total) return;
+  {
+    float* z = dq_acc + row * D + lane * (D / 32);
+    if constexpr (D == 128)
+      *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else
+      *reinterpret_cast<float2*>(z) = make_float2(0.f, 0.f);
+  }
   constexpr int E = D / 32;  // elements per lane (2 or 4)
   const __nv_bfloat16* op = o + row * D + lane * E;
   const __nv_bfloat16* gp = g_o + row * D + lane * E;
@@ -304,18 +316,16 @@ cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void
                        void* g_v, float* ws_D, float* ws_dq, int32_t* ws_status,
                        cudaStream_t st) {
   const int64_t rows = (int64_t)sh.B * sh.n * sh.H;
-  cudaError_t e = cudaMemsetAsync(ws_dq, 0, (size_t)rows * sh.d * sizeof(float), st);
-  if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(ws_status, 0, sizeof(int32_t), st);
-  if (e != cudaSuccess) return e;
   unsigned pre_blocks = (unsigned)((rows + 7) / 8);
   if (sh.d == 64)
     bwd_pre_kernel<64><<<pre_blocks, 256, 0, st>>>((const __nv_bfloat16*)o,
-                                                   (const __nv_bfloat16*)g_o, ws_D, sh);
+                                                   (const __nv_bfloat16*)g_o, ws_D, ws_dq,
+                                                   ws_status, sh);
   else
     bwd_pre_kernel<128><<<pre_blocks, 256, 0, st>>>((const __nv_bfloat16*)o,
-                                                    (const __nv_bfloat16*)g_o, ws_D, sh);
-  e = cudaGetLastError();
+                                                    (const __nv_bfloat16*)g_o, ws_D, ws_dq,
+                                                    ws_status, sh);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (bwd_tc_supported(sh))
     e = launch_bwd_tc(sh, q, k, v, g_o, lse, ws_D, q_idx, q_cnt, g_k, g_v, ws_dq, ws_status,

@@ -69,10 +69,10 @@ extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, c
   sh.T_r = (sh.n + sh.block_q - 1) / sh.block_q;
   sh.T_c = (sh.n + sh.block_k - 1) / sh.block_k;
   sh.n_pad = (int64_t)sh.T_r * sh.block_q;
-  // Same layout as the workspace of bl_attn_bwd.  launch_bwd zeroes the dQ
-  // accumulator and the status word on the stream before its kernels run, and
-  // the preprocessing kernel writes every D entry, so nothing left by an
-  // earlier call leaks into this one.
+  // Same layout as the workspace of bl_attn_bwd.  The preprocessing kernel
+  // that launch_bwd runs first writes every D entry and zeroes the dQ
+  // accumulator and the status word, so nothing left by an earlier call leaks
+  // into this one.
   const size_t d_bytes = round256((size_t)sh.B * sh.H * sh.n * sizeof(float));
   const size_t dq_bytes = (size_t)sh.B * sh.n * sh.H * sh.d * sizeof(float);
   float* ws_D = reinterpret_cast<float*>(ws);

@@ -93,31 +93,43 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
     lrow[e] = valid[e] ? lse[bh * sh.n + r0 + e] : 0.f;
   }
   const float* st = stats + bh * sh.T_c * sh.n_pad + r0;
-  for (int j = warp; j < Tc; j += kMaskThreads / 32) {
-    float vals[RPL];
-    if constexpr (RPL == 4) {
-      float4 x = *reinterpret_cast<const float4*>(st + (int64_t)j * sh.n_pad);
-      vals[0] = x.x; vals[1] = x.y; vals[2] = x.z; vals[3] = x.w;
-    } else {
-      float2 x = *reinterpret_cast<const float2*>(st + (int64_t)j * sh.n_pad);
-      vals[0] = x.x; vals[1] = x.y;
-    }
-    float mx = -INFINITY;
-    bool nan = false;
+  constexpr int NW = kMaskThreads / 32;
+  constexpr int UNR = 4;   // key tiles in flight per warp
+  for (int j0 = warp; j0 < Tc; j0 += NW * UNR) {
+    float vals[UNR][RPL];
 #pragma unroll
-    for (int e = 0; e < RPL; ++e) {
-      if (!valid[e]) continue;
-      float dv = __fsub_rn(vals[e], lrow[e]);
-      if (isnan(dv)) nan = true;
-      else mx = fmaxf(mx, dv);
+    for (int u = 0; u < UNR; ++u) {
+      const int j = j0 + u * NW;
+      if (j >= Tc) continue;
+      if constexpr (RPL == 4) {
+        float4 x = *reinterpret_cast<const float4*>(st + (int64_t)j * sh.n_pad);
+        vals[u][0] = x.x; vals[u][1] = x.y; vals[u][2] = x.z; vals[u][3] = x.w;
+      } else {
+        float2 x = *reinterpret_cast<const float2*>(st + (int64_t)j * sh.n_pad);
+        vals[u][0] = x.x; vals[u][1] = x.y;
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    bool any_nan = __any_sync(0xffffffffu, nan);
-    if (lane == 0) {
-      float dv = any_nan ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
-      if (dv == 0.f) dv = 0.f;  // -0 -> +0
-      s_d[j] = dv;
+    for (int u = 0; u < UNR; ++u) {
+      const int j = j0 + u * NW;
+      if (j >= Tc) continue;   // warp-uniform
+      float mx = -INFINITY;
+      bool nan = false;
+#pragma unroll
+      for (int e = 0; e < RPL; ++e) {
+        if (!valid[e]) continue;
+        float dv = __fsub_rn(vals[u][e], lrow[e]);
+        if (isnan(dv)) nan = true;
+        else mx = fmaxf(mx, dv);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      bool any_nan = __any_sync(0xffffffffu, nan);
+      if (lane == 0) {
+        float dv = any_nan ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
+        if (dv == 0.f) dv = 0.f;  // -0 -> +0
+        s_d[j] = dv;
+      }
     }
   }
   __syncthreads();
