@@ -138,7 +138,8 @@ template <int D>
 __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_gk,
+    const __grid_constant__ CUtensorMap tm_gv, const float* __restrict__ lse,
     const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
     const int32_t* __restrict__ q_cnt, __nv_bfloat16* __restrict__ g_k,
     __nv_bfloat16* __restrict__ g_v, int32_t* __restrict__ status, Shape sh, float scale,
@@ -170,6 +171,16 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     mbar_init(&bars.acc, 1);
     s_fail = 0;
     fence_mbar_init();
+    // K_j, V_j start loading before the lists are copied and TMEM allocated
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_g);
+    mbar_expect_tx(&bars.kv, 2 * C::TILE);
+    for (int c = 0; c < C::CHK; ++c) {
+      tma_load_4d(sm + C::OFF_K + c * C::CHUNK, &tm_k, &bars.kv, c * 64, hk, j * 128, b);
+      tma_load_4d(sm + C::OFF_V + c * C::CHUNK, &tm_v, &bars.kv, c * 64, hk, j * 128, b);
+    }
   }
   if (warp == 1) tmem_alloc(&s_tmem, C::T_COLS);
   int32_t* s_list = reinterpret_cast<int32_t*>(sm + C::OFF_LIST);
@@ -223,17 +234,6 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
    if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_g);
-      mbar_expect_tx(&bars.kv, 2 * C::TILE);
-      for (int c = 0; c < C::CHK; ++c) {
-        tma_load_4d(sm + C::OFF_K + c * C::CHUNK, &tm_k, &bars.kv, c * 64, hk, j * 128, b);
-        tma_load_4d(sm + C::OFF_V + c * C::CHUNK, &tm_v, &bars.kv, c * 64, hk, j * 128, b);
-      }
-    }
     int x = 0;   // load index: 2t for Q of tile t, 2t+1 for its dO
     bool ok = true;
     while (ok && walk.next()) {
@@ -431,10 +431,12 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const bool acc_ok = mbar_wait(&bars.acc, 0);
     fence_after_sync();
     const bool have = __all_sync(0xffffffffu, ok && acc_ok) && t > 0;
-    const int key = j * 128 + r;
-    __nv_bfloat16* dst = (half == 0 ? g_v : g_k) + (((int64_t)b * sh.n + key) * sh.Hk + hk) * D;
+    // Stage the bf16 rows in ring slot `half` (free: every load has been
+    // consumed by the finished MMAs) with the 128-byte swizzle and store them
+    // with TMA, which drops rows past n.
     const float mul = half == 0 ? 1.f : scale;
     const uint32_t col = half == 0 ? C::T_DV : C::T_DK;
+    uint8_t* stg = sm + C::OFF_RING + half * C::TILE;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t a[32];
@@ -442,19 +444,27 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         tmem_ld32(lane_base + col + c0, a);
         tmem_ld_wait();
       }
-      if (key < sh.n) {
+      uint8_t* row_base = stg + (c0 >> 6) * C::CHUNK + r * 128;
 #pragma unroll
-        for (int x8 = 0; x8 < 32; x8 += 8) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (have)
-            w = make_uint4(
-                pack_bf16(__uint_as_float(a[x8]) * mul, __uint_as_float(a[x8 + 1]) * mul),
-                pack_bf16(__uint_as_float(a[x8 + 2]) * mul, __uint_as_float(a[x8 + 3]) * mul),
-                pack_bf16(__uint_as_float(a[x8 + 4]) * mul, __uint_as_float(a[x8 + 5]) * mul),
-                pack_bf16(__uint_as_float(a[x8 + 6]) * mul, __uint_as_float(a[x8 + 7]) * mul));
-          *reinterpret_cast<uint4*>(dst + c0 + x8) = w;
-        }
+      for (int x8 = 0; x8 < 32; x8 += 8) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (have)
+          w = make_uint4(
+              pack_bf16(__uint_as_float(a[x8]) * mul, __uint_as_float(a[x8 + 1]) * mul),
+              pack_bf16(__uint_as_float(a[x8 + 2]) * mul, __uint_as_float(a[x8 + 3]) * mul),
+              pack_bf16(__uint_as_float(a[x8 + 4]) * mul, __uint_as_float(a[x8 + 5]) * mul),
+              pack_bf16(__uint_as_float(a[x8 + 6]) * mul, __uint_as_float(a[x8 + 7]) * mul));
+        const int piece = ((c0 & 63) + x8) >> 3;     // 16-byte chunk within the 128-byte row
+        *reinterpret_cast<uint4*>(row_base + ((piece ^ (r & 7)) << 4)) = w;
       }
+    }
+    fence_async_smem();
+    named_sync(3 + half, 128);
+    if (q4 == 0 && lane == 0) {
+      for (int c = 0; c < C::CHK; ++c)
+        tma_store_4d(half == 0 ? &tm_gv : &tm_gk, stg + c * C::CHUNK, c * 64, hk, j * 128, b);
+      bulk_commit();
+      bulk_wait_read0();
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
@@ -500,7 +510,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       }
       ++u;
     }
-    if (dt == 0) bulk_wait0();
+    if (dt == 0) bulk_wait_read0();   // the staging rows must outlive the reads
     if (!ok && lane == 0) fail();
   }
 
@@ -515,19 +525,21 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
                      const int32_t* q_cnt, void* g_k, void* g_v, float* dq_acc, int32_t* status,
                      float scale, cudaStream_t st) {
   using C = Cfg<D>;
-  CUtensorMap mq, mk, mv, mg, md;
+  CUtensorMap mq, mk, mv, mg, md, mgk, mgv;
   if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
       !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 128) ||
       !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) ||
       !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
-      !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
+      !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128) ||
+      !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 128) ||
+      !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
   auto kern = bwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(sh.T_c, sh.Hk, sh.B);
-  kern<<<grid, 512, smem, st>>>(mq, mk, mv, mg, md, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
+  kern<<<grid, 512, smem, st>>>(mq, mk, mv, mg, md, mgk, mgv, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
                                 (__nv_bfloat16*)g_v, status, sh, scale, scale * kLog2e);
   return cudaGetLastError();
 }

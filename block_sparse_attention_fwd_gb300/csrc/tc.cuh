@@ -106,6 +106,16 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, const vo
       "r"(saddr(src)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
+// Bulk tensor store shared -> global; rows past the tensor's extent are
+// dropped by the TMA unit.  Coordinates must be non-negative.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* src, int x, int y,
+                                             int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
+          "l"(m),
+      "r"(saddr(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
