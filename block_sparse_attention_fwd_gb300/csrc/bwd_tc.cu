@@ -337,18 +337,25 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
                  (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.empty[(2 * t) % C::NS]);
         mma_commit(&bars.empty[(2 * t + 1) % C::NS]);
+        // S^T of the next tile goes ahead of dQ so that the first softmax phase
+        // of that tile overlaps the dQ product and its drain.  It is queued
+        // behind dV, which read P^T from R_S.
+        have = walk.next();
+        if (have) {
+          ok = wait_slot(2 * (t + 1));
+          if (!ok) break;
+          fence_after_sync();
+          issue_s(t + 1);
+        }
         // dQ = dS K into R_dP (dP^T was consumed by the softmax)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + C::T_DP, sdesc_sw128(sDS + kk * 2048, C::CHUNK, 1024),
                  sdesc_sw128(sK + kk * 2048, C::CHUNK, 1024), C::ID_Q, kk > 0 ? 1u : 0u);
         mma_commit(&bars.dq_ready);
-        have = walk.next();
         if (have) {
-          ok = wait_slot(2 * (t + 1));
-          if (!ok) break;
-          fence_after_sync();
-          issue_s(t + 1);                     // queued behind dV and dQ of tile t
+          // dP^T of the next tile once the dQ tile has left R_dP; the dS^T
+          // buffer is rewritten only after dP^T completes, hence after dQ
           ok = mbar_wait(&bars.dq_free, t & 1) && wait_slot(2 * (t + 1) + 1);
           if (!ok) break;
           fence_after_sync();
@@ -372,46 +379,60 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     bool ok = true;
     while (ok && walk.next()) {
       const int s = (2 * t) % C::NS;
+      // phase 1: P^T from S^T (needs only S^T), written back over S^T
       ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
                                        mbar_wait(&bars.full[s], ((2 * t) / C::NS) & 1) &&
-                                       mbar_wait(&bars.s_full, t & 1) &&
-                                       mbar_wait(&bars.dp_full, t & 1));
+                                       mbar_wait(&bars.s_full, t & 1));
       if (!ok) break;
       fence_after_sync();
       const float* sl = reinterpret_cast<const float*>(sm + C::OFF_L) + s * 128 + half * 64;
       const float* sd = reinterpret_cast<const float*>(sm + C::OFF_D) + s * 128 + half * 64;
+      float pf[64];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {    // 32 query columns per pass
-        const int cb = half * 64 + pass * 32;
-        uint32_t sv[32], pv[32];
-        tmem_ld32(lane_base + C::T_S + cb, sv);
-        tmem_ld32(lane_base + C::T_DP + cb, pv);
+        uint32_t sv[32];
+        tmem_ld32(lane_base + C::T_S + half * 64 + pass * 32, sv);
         tmem_ld_wait();
-        float lrow[32], drow[32];
+        uint32_t pk[16];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 a = reinterpret_cast<const float4*>(sl + pass * 32)[c4];
-          const float4 d4 = reinterpret_cast<const float4*>(sd + pass * 32)[c4];
-          lrow[4 * c4] = a.x; lrow[4 * c4 + 1] = a.y; lrow[4 * c4 + 2] = a.z; lrow[4 * c4 + 3] = a.w;
-          drow[4 * c4] = d4.x; drow[4 * c4 + 1] = d4.y; drow[4 * c4 + 2] = d4.z; drow[4 * c4 + 3] = d4.w;
-        }
-        uint32_t pk[16], dk[16];
+          const float4 l4 = reinterpret_cast<const float4*>(sl + pass * 32)[c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p2[2], d2[2];
-#pragma unroll
-          for (int y = 0; y < 2; ++y) {
-            const int c = 2 * e + y;
-            const float p =
-                key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lrow[c])) : 0.f;
-            p2[y] = p;
-            d2[y] = p * (__uint_as_float(pv[c]) - drow[c]);
+          for (int y = 0; y < 4; ++y) {
+            const int c = 4 * c4 + y;
+            pf[pass * 32 + c] =
+                key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
           }
-          pk[e] = pack_bf16(p2[0], p2[1]);
-          dk[e] = pack_bf16(d2[0], d2[1]);
+          pk[2 * c4] = pack_bf16(pf[pass * 32 + 4 * c4], pf[pass * 32 + 4 * c4 + 1]);
+          pk[2 * c4 + 1] = pack_bf16(pf[pass * 32 + 4 * c4 + 2], pf[pass * 32 + 4 * c4 + 3]);
         }
         // P^T pairs over this warpgroup's own S^T columns (already read)
         tmem_st16(lane_base + C::T_S + half * 64 + pass * 16, pk);
+      }
+      // phase 2: dS^T = P^T (dP^T - D) once dP^T has landed
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, t & 1));
+      if (!ok) break;
+      fence_after_sync();
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        uint32_t pv[32];
+        tmem_ld32(lane_base + C::T_DP + half * 64 + pass * 32, pv);
+        tmem_ld_wait();
+        uint32_t dk[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = reinterpret_cast<const float4*>(sd + pass * 32)[c4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float ds[4];
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const int c = 4 * c4 + y;
+            ds[y] = pf[pass * 32 + c] * (__uint_as_float(pv[c]) - dv[y]);
+          }
+          dk[2 * c4] = pack_bf16(ds[0], ds[1]);
+          dk[2 * c4 + 1] = pack_bf16(ds[2], ds[3]);
+        }
         // dS^T, K-major [key][q] with the 128-byte swizzle, 4 x 16 B chunks
 #pragma unroll
         for (int c16 = 0; c16 < 4; ++c16) {
