@@ -530,6 +530,21 @@ def run_all_configs(args):
                 line["oracle_bwd_ms_extrapolated"] = ms_cpu
                 line["oracle_sample"] = f"{tiles} query tiles in {el:.1f} s, {os.cpu_count()} cores"
             print(json.dumps(line), flush=True)
+        if name == "video_n32760_d128":
+            # LSE-combine of two partial results of this shape (HBM-bound)
+            parts = 2
+            op = torch.empty((parts,) + tuple(o.shape), dtype=torch.bfloat16, device=dev)
+            op[0].copy_(o)
+            op[1].copy_(o)
+            lp = torch.stack([lse, lse]).contiguous()
+            oc, lc = torch.empty_like(o), torch.empty_like(lse)
+            cm = timed(lambda: _lib.lse_combine(op, lp, oc, lc), reps)
+            rows = w.B * w.n * w.H
+            nbytes = parts * rows * (2 * w.d + 4) + rows * (2 * w.d + 4)
+            print(json.dumps({"workload": name, "kernel": "bl_lse_combine", "parts": parts,
+                              "ms": cm, "gbs": nbytes / cm / 1e6,
+                              "frac_hbm": nbytes / cm / 1e6 / pk["hbm"]}), flush=True)
+            del op, lp, oc, lc
         del qd, kd, vd, god, o, lse, stats, lists, g_q, g_k, g_v, wsb
         torch.cuda.empty_cache()
     return 0

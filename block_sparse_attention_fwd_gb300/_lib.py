@@ -21,7 +21,7 @@ BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "B
 # Every symbol include/bl_attn.h declares (checked by the CPU test suite).
 EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
            "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
-           "bl_attn_bwd_noalloc")
+           "bl_attn_bwd_noalloc", "bl_lse_combine")
 
 
 class Shape(ctypes.Structure):
@@ -68,6 +68,8 @@ def load():
     lib.bl_attn_bwd.restype = ctypes.c_int
     lib.bl_attn_bwd_noalloc.argtypes = [S, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P, P]
     lib.bl_attn_bwd_noalloc.restype = ctypes.c_int
+    lib.bl_lse_combine.argtypes = [ctypes.c_int] * 5 + [P, P, P, P, P]
+    lib.bl_lse_combine.restype = ctypes.c_int
     lib.bl_bwd_check_status.argtypes = [S, P, P]
     lib.bl_bwd_check_status.restype = ctypes.c_int
     lib.bl_status_string.argtypes = [ctypes.c_int]
@@ -212,3 +214,16 @@ def attn_bwd_noalloc(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v):
                                       ctypes.byref(ls) if ls is not None else None,
                                       _ptr(g_q), _ptr(g_k), _ptr(g_v), _stream(q.device))
     _check("bl_attn_bwd_noalloc", code)
+
+
+def lse_combine(o_parts, lse_parts, o, lse):
+    """bl_lse_combine: o_parts [P,B,n,H,d] bf16, lse_parts [P,B,H,n] fp32 ->
+    o [B,n,H,d] bf16, lse [B,H,n] fp32."""
+    P, B, n, H, d = o_parts.shape
+    _need(o_parts, torch.bfloat16, (P, B, n, H, d), "o_parts")
+    _need(lse_parts, torch.float32, (P, B, H, n), "lse_parts")
+    _need(o, torch.bfloat16, (B, n, H, d), "o")
+    _need(lse, torch.float32, (B, H, n), "lse")
+    code = load().bl_lse_combine(P, B, n, H, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o),
+                                 _ptr(lse), _stream(o.device))
+    _check("bl_lse_combine", code)

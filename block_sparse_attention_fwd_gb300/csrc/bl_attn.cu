@@ -125,6 +125,17 @@ bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace, void
   return (host & 1) ? BL_ERR_CORRUPT_LISTS : BL_OK;
 }
 
+bl_status bl_lse_combine(int parts, int B, int n, int H, int d, const void* o_parts,
+                         const float* lse_parts, void* o, float* lse, void* stream) {
+  if (parts < 1 || parts > 32 || B < 1 || n < 1 || H < 1) return BL_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return BL_ERR_UNSUPPORTED;
+  if (!o_parts || !lse_parts || !o || !lse) return BL_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse))
+    return BL_ERR_INVALID_ARG;
+  return cuda_status(bl::launch_combine(parts, B, n, H, d, o_parts, lse_parts, o, lse,
+                                        (cudaStream_t)stream));
+}
+
 const char* bl_status_string(bl_status status) {
   switch (status) {
     case BL_OK: return "ok";

@@ -41,6 +41,10 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
                           float* lse, float* stats, int32_t* status, float scale,
                           cudaStream_t st);
 
+// LSE-combine of `parts` partial results (layouts in include/bl_attn.h).
+cudaError_t launch_combine(int parts, int B, int n, int H, int d, const void* o_parts,
+                           const float* lse_parts, void* o, float* lse, cudaStream_t st);
+
 // 4-D TMA map of a BSHD bf16 tensor [B][n][heads][d]: box of 64 elements of d
 // x 1 head x `rows` tokens x 1 batch, 128-byte swizzle, out-of-range reads 0.
 bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows);

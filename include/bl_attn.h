@@ -147,6 +147,19 @@ bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k,
 bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace,
                               void* stream);
 
+/* LSE-combine ("BackLite" README, Key properties: the LSE output serves to
+ * combine partial attention results).  Given `parts` results of the same
+ * queries over disjoint key sets,
+ *   o_parts   [parts, B, n, H, d] bf16   (each part laid out like o)
+ *   lse_parts [parts, B, H, n]    fp32   (each part laid out like lse)
+ * writes LSE = log sum_p exp(LSE_p) and O = sum_p exp(LSE_p - LSE) O_p into
+ * o [B, n, H, d] bf16 and lse [B, H, n] fp32.  A part whose LSE is -inf (it
+ * saw no key) carries no weight; a row with no finite part gets O = 0 and
+ * LSE = -inf.  parts in [1, 32], d in {64, 128}.
+ * Errors: BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED, BL_ERR_CUDA. */
+bl_status bl_lse_combine(int parts, int B, int n, int H, int d, const void* o_parts,
+                         const float* lse_parts, void* o, float* lse, void* stream);
+
 /* Size of the fixed device scratch array behind bl_attn_bwd_noalloc: 32 MiB
  * on every GPU that loads the library, held until the process exits. */
 #define BL_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

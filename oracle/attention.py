@@ -217,3 +217,49 @@ def backward(q, k, v, o, g_o, lse, scale, tile_masks=None, block_q=None,
             gk[b, :, hk] += bk
             gv[b, :, hk] += bv
     return gq, gk, gv
+
+
+def combine(o_parts, lse_parts):
+    """Merge partial attention results over disjoint key sets ("BackLite"
+    README, Key properties: the LSE output serves to combine partial results).
+
+    o_parts [P, B, n, H, d], lse_parts [P, B, H, n] (natural log) ->
+    O = sum_p exp(LSE_p - LSE) O_p with LSE = log sum_p exp(LSE_p).
+    Parts with LSE -inf carry no weight; rows where every part is -inf get
+    O = 0 and LSE = -inf.
+    """
+    o_parts = _f64(o_parts)
+    lse_parts = _f64(lse_parts)
+    m = lse_parts.max(axis=0)                               # [B, H, n]
+    finite = np.isfinite(m)
+    mm = np.where(finite, m, 0.0)
+    with np.errstate(invalid="ignore"):
+        w = np.exp(lse_parts - mm[None])                    # [P, B, H, n]
+    w = np.where(np.isfinite(lse_parts), w, 0.0)
+    tot = w.sum(axis=0)
+    lse = np.where(finite, mm + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    wn = np.where(tot[None] > 0, w / np.where(tot > 0, tot, 1.0)[None], 0.0)
+    # weights are per (b, h, row); outputs are (b, row, h, d)
+    o = np.einsum("pbhn,pbnhd->bnhd", wn, o_parts)
+    return o, lse
+
+
+def forward_keys(q, k, v, scale, keys):
+    """Exact attention of every query over the key subset `keys` only:
+    O [B,n,H,d] and LSE [B,H,n] (-inf where the subset is empty)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, n, H, d = q.shape
+    Hk = k.shape[2]
+    keys = np.asarray(keys)
+    O = np.zeros((B, n, H, d))
+    L = np.full((B, H, n), -np.inf)
+    if len(keys) == 0:
+        return O, L
+    for b in range(B):
+        for h in range(H):
+            hk = kv_head(h, H, Hk)
+            S = scores(q[b, :, h], k[b, keys, hk], scale)
+            _, P, lse = row_softmax_stats(S)
+            O[b, :, h] = P @ v[b, keys, hk]
+            L[b, h] = lse
+    return O, L

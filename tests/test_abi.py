@@ -110,3 +110,11 @@ def test_product_path_never_imports_the_oracle():
             if f.endswith(".py"):
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle", src, re.M), f
+
+
+def test_combine_rejects_bad_arguments(lib):
+    ok = ctypes.c_void_p(0x10000)
+    assert lib.bl_lse_combine(0, 1, 8, 1, 64, ok, ok, ok, ok, None) == 1
+    assert lib.bl_lse_combine(33, 1, 8, 1, 64, ok, ok, ok, ok, None) == 1
+    assert lib.bl_lse_combine(2, 1, 8, 1, 96, ok, ok, ok, ok, None) == 2
+    assert lib.bl_lse_combine(2, 1, 8, 1, 64, None, ok, ok, ok, None) == 1

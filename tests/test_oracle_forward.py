@@ -105,3 +105,27 @@ def test_underflowing_tile_is_minus_inf():
     assert np.all(st[0, 0, 0, :n] == -np.inf)
     assert np.allclose(st[0, 0, 1, :n], math.log(4.0))
     assert np.allclose(L, math.log(4.0))
+
+
+@pytest.mark.parametrize("cuts", [[0, 13, 40], [0, 1, 2, 40], [0, 40, 40]])
+def test_combine_of_a_key_partition_is_the_full_attention(cuts):
+    """Splitting the keys into disjoint sets and combining the partial results
+    with their LSEs gives the full attention (and an empty part is ignored)."""
+    n, d = 40, 8
+    q, k, v = _rand((2, n, 4, d), 21), _rand((2, n, 2, d), 22), _rand((2, n, 2, d), 23)
+    scale = 0.4
+    O, L, _ = A.forward(q, k, v, scale)
+    parts = [A.forward_keys(q, k, v, scale, np.arange(a, b)) for a, b in zip(cuts[:-1], cuts[1:])]
+    Oc, Lc = A.combine(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    assert np.allclose(Oc, O, atol=1e-13) and np.allclose(Lc, L, atol=1e-13)
+
+
+def test_combine_closed_form_and_empty_rows():
+    o = np.zeros((2, 1, 1, 1, 2))
+    o[0, 0, 0, 0] = [1.0, 0.0]
+    o[1, 0, 0, 0] = [0.0, 1.0]
+    lse = np.array([math.log(1.0), math.log(3.0)]).reshape(2, 1, 1, 1)
+    Oc, Lc = A.combine(o, lse)
+    assert np.allclose(Oc[0, 0, 0], [0.25, 0.75]) and abs(Lc[0, 0, 0] - math.log(4.0)) < 1e-15
+    Oe, Le = A.combine(o, np.full((2, 1, 1, 1), -np.inf))
+    assert np.all(Oe == 0) and Le[0, 0, 0] == -np.inf
