@@ -55,9 +55,29 @@ def kv_head(h: int, H: int, Hk: int) -> int:
     return h // (H // Hk)
 
 
-def scores(q_rows: np.ndarray, k_head: np.ndarray, scale: float) -> np.ndarray:
-    """S = s * Q K^T for the given query rows against every key: [r, n]."""
-    return scale * (q_rows @ k_head.T)
+def allowed(rows, cols, causal=False, window=0) -> np.ndarray:
+    """Structural mask of the (query row, key) pairs that attend: causal keeps
+    keys c <= r; a sliding window of W (with causal) keeps r - W < c <= r.
+    Reading adopted for the sliding-window attention the BackLite blog trains
+    with (Nanochat: windows of 1024 and 2048): W counts the query's own key."""
+    r = np.asarray(rows)[:, None]
+    c = np.asarray(cols)[None, :]
+    ok = np.ones((r.shape[0], c.shape[1]), dtype=bool)
+    if causal:
+        ok &= c <= r
+    if window:
+        ok &= c > r - window
+    return ok
+
+
+def scores(q_rows: np.ndarray, k_head: np.ndarray, scale: float, rows=None, cols=None,
+           causal=False, window=0) -> np.ndarray:
+    """S = s * Q K^T for the given query rows against the given keys: [r, c];
+    pairs the structural mask removes are -inf."""
+    S = scale * (q_rows @ k_head.T)
+    if causal or window:
+        S = np.where(allowed(rows, cols, causal, window), S, -np.inf)
+    return S
 
 
 def row_softmax_stats(S: np.ndarray):
@@ -85,7 +105,7 @@ def tile_lse(S: np.ndarray, block_k: int) -> np.ndarray:
     return out.T.copy()
 
 
-def forward_head(q_h, k_h, v_h, scale, rows=None, block_k=None):
+def forward_head(q_h, k_h, v_h, scale, rows=None, block_k=None, causal=False, window=0):
     """Exact attention for one (batch, head).
 
     q_h [n, d], k_h/v_h [n, d] fp64.  ``rows``: query row indices (default all).
@@ -96,7 +116,7 @@ def forward_head(q_h, k_h, v_h, scale, rows=None, block_k=None):
     outs_o, outs_l, outs_t = [], [], []
     for g in range(0, len(rows), ROW_GROUP):
         rr = rows[g:g + ROW_GROUP]
-        S = scores(q_h[rr], k_h, scale)
+        S = scores(q_h[rr], k_h, scale, rr, np.arange(n), causal, window)
         _, P, lse = row_softmax_stats(S)
         outs_o.append(P @ v_h)
         outs_l.append(lse)
@@ -108,7 +128,7 @@ def forward_head(q_h, k_h, v_h, scale, rows=None, block_k=None):
     return O, L, T
 
 
-def forward(q, k, v, scale, block_q=None, block_k=None):
+def forward(q, k, v, scale, block_q=None, block_k=None, causal=False, window=0):
     """Exact attention over BSHD tensors.
 
     q [B,n,H,d], k/v [B,n,Hk,d] -> O [B,n,H,d] fp64, LSE [B,H,n] fp64 and, when
@@ -127,7 +147,7 @@ def forward(q, k, v, scale, block_q=None, block_k=None):
         for h in range(H):
             hk = kv_head(h, H, Hk)
             o, l, t = forward_head(q[b, :, h], k[b, :, hk], v[b, :, hk], scale,
-                                   block_k=block_k)
+                                   block_k=block_k, causal=causal, window=window)
             O[b, :, h] = o
             LSE[b, h] = l
             if stats is not None:
@@ -152,7 +172,7 @@ def element_mask(tile_mask: np.ndarray, block_q: int, block_k: int,
 
 
 def backward_head(q_h, k_h, v_h, o_h, go_h, lse_h, scale, tile_mask,
-                  block_q, block_k, rows=None, cols=None):
+                  block_q, block_k, rows=None, cols=None, causal=False, window=0):
     """Masked attention backward for one (batch, query head).
 
     With P the exact softmax (recomputed from the full-row LSE) and M the
@@ -176,7 +196,7 @@ def backward_head(q_h, k_h, v_h, o_h, go_h, lse_h, scale, tile_mask,
     k_c, v_c = k_h[cols], v_h[cols]
     for g in range(0, len(rows), ROW_GROUP):
         rr = rows[g:g + ROW_GROUP]
-        S = scores(q_h[rr], k_c, scale)
+        S = scores(q_h[rr], k_c, scale, rr, cols, causal, window)
         P = np.exp(S - lse_h[rr][:, None])
         if tile_mask is not None:
             P = P * element_mask(tile_mask, block_q, block_k, rr, cols)
@@ -190,7 +210,7 @@ def backward_head(q_h, k_h, v_h, o_h, go_h, lse_h, scale, tile_mask,
 
 
 def backward(q, k, v, o, g_o, lse, scale, tile_masks=None, block_q=None,
-             block_k=None):
+             block_k=None, causal=False, window=0):
     """Masked attention backward over BSHD tensors (full, every row/column).
 
     ``tile_masks``: [B, H, T_r, T_c] (nonzero = compute), or None for dense.
@@ -212,7 +232,7 @@ def backward(q, k, v, o, g_o, lse, scale, tile_masks=None, block_q=None,
             tm = None if tile_masks is None else np.asarray(tile_masks[b, h])
             a, bk, bv = backward_head(q[b, :, h], k[b, :, hk], v[b, :, hk],
                                       o[b, :, h], g_o[b, :, h], lse[b, h], scale,
-                                      tm, block_q, block_k)
+                                      tm, block_q, block_k, causal=causal, window=window)
             gq[b, :, h] = a
             gk[b, :, hk] += bk
             gv[b, :, hk] += bv

@@ -33,7 +33,11 @@ selection, the tie-break nor the arithmetic.  Readings adopted:
    ascending).  The skipped set is the longest prefix of that order whose
    running integer sum of E stays < T; everything else is active.  A NaN d
    keeps its tile active and is counted.
-5. Outputs per (b, h): mask [T_r, T_c] uint8 (1 = compute), kv_idx
+5. With a causal or sliding-window structure, a tile none of whose (query,
+   key) pairs attends is never kept, whatever negl_prob (it has nothing to
+   compute; its weight is 0, so with negl_prob > 0 the rule above already
+   skips it).
+6. Outputs per (b, h): mask [T_r, T_c] uint8 (1 = compute), kv_idx
    [T_r, T_c] int32 (active key tiles ascending, then -1), kv_cnt [T_r],
    q_idx [T_c, T_r] int32 (active query tiles ascending, then -1), q_cnt [T_c].
 
@@ -134,7 +138,27 @@ def select_row(d_row: np.ndarray, T: int):
     return active, int(nan.sum())
 
 
-def mask_from_stats(stats, lse, n, block_q, block_k, negl_prob):
+def structurally_empty(T_r, T_c, n, block_q, block_k, causal=False, window=0):
+    """[T_r, T_c] bool: tiles in which no (query, key) pair attends."""
+    empty = np.zeros((T_r, T_c), dtype=bool)
+    if not (causal or window):
+        return empty
+    for i in range(T_r):
+        r0, r1 = i * block_q, min(n, (i + 1) * block_q) - 1
+        for j in range(T_c):
+            c0, c1 = j * block_k, min(n, (j + 1) * block_k) - 1
+            # some pair attends iff the lowest key is <= the highest row (causal)
+            # and the highest key is > the lowest row - window (window)
+            some = True
+            if causal:
+                some &= c0 <= r1
+            if window:
+                some &= c1 > r0 - window
+            empty[i, j] = not some
+    return empty
+
+
+def mask_from_stats(stats, lse, n, block_q, block_k, negl_prob, causal=False, window=0):
     """Apply the rule to fp32 stats [B,H,T_c,n_pad] and fp32 LSE [B,H,n].
 
     Returns a dict of numpy arrays: mask, kv_idx, kv_cnt, q_idx, q_cnt, and the
@@ -147,12 +171,14 @@ def mask_from_stats(stats, lse, n, block_q, block_k, negl_prob):
     T = threshold(negl_prob)
     mask = np.ones((B, H, T_r, T_c), dtype=np.uint8)
     nan_total = 0
+    empty = structurally_empty(T_r, T_c, n, block_q, block_k, causal, window)
     for b in range(B):
         for h in range(H):
             d = tile_weights(stats[b, h], lse[b, h], n, block_q)
             for i in range(T_r):
                 mask[b, h, i], c = select_row(d[i], T)
                 nan_total += c
+            mask[b, h][empty] = 0
     return lists_from_mask(mask) | {"nan_count": nan_total}
 
 

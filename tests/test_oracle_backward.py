@@ -141,3 +141,22 @@ def test_stored_output_is_bf16_round_to_nearest_even():
     y = A.as_stored_output(x)
     assert y[0, 0] == 1.0 and y[0, 1] == 1.0 + 2.0 ** -6
     assert abs(y[0, 3] - 0.1) <= 0.1 * 2.0 ** -9
+
+
+@pytest.mark.parametrize("window", [0, 6])
+def test_causal_window_gradient_matches_torch_autograd(window):
+    B, n, H, Hk, d = 1, 23, 2, 1, 4
+    q, k, v, go = _problem(B, n, H, Hk, d, seed=41)
+    scale = 0.5
+    O, L, _ = A.forward(q, k, v, scale, causal=True, window=window)
+    gq, gk, gv = A.backward(q, k, v, O, go, L, scale, causal=True, window=window)
+    tq, tk, tv = (torch.from_numpy(x).clone().requires_grad_(True) for x in (q, k, v))
+    r = torch.arange(n)[:, None]
+    c = torch.arange(n)[None, :]
+    m = (c <= r) & ((c > r - window) if window else torch.ones_like(c <= r))
+    S = scale * torch.einsum("bnhd,bmhd->bhnm", tq, tk.repeat_interleave(2, dim=2))
+    S = S.masked_fill(~m, float("-inf"))
+    O_t = torch.einsum("bhnm,bmhd->bnhd", torch.softmax(S, dim=-1), tv.repeat_interleave(2, dim=2))
+    O_t.backward(torch.from_numpy(go))
+    for mine, ref in ((gq, tq.grad), (gk, tk.grad), (gv, tv.grad)):
+        assert np.allclose(mine, ref.numpy(), rtol=0, atol=1e-12)

@@ -129,3 +129,31 @@ def test_combine_closed_form_and_empty_rows():
     assert np.allclose(Oc[0, 0, 0], [0.25, 0.75]) and abs(Lc[0, 0, 0] - math.log(4.0)) < 1e-15
     Oe, Le = A.combine(o, np.full((2, 1, 1, 1), -np.inf))
     assert np.all(Oe == 0) and Le[0, 0, 0] == -np.inf
+
+
+@pytest.mark.parametrize("window", [0, 5, 17])
+def test_causal_and_window_forward_match_torch(window):
+    """Causal (and causal sliding-window) attention against fp64 torch SDPA with
+    an explicit boolean mask; tile statistics keep their partition invariant."""
+    B, n, H, Hk, d = 1, 37, 2, 1, 8
+    q, k, v = _rand((B, n, H, d), 31), _rand((B, n, Hk, d), 32), _rand((B, n, Hk, d), 33)
+    scale = 0.45
+    O, L, st = A.forward(q, k, v, scale, block_q=8, block_k=8, causal=True, window=window)
+    r = np.arange(n)[:, None]
+    c = np.arange(n)[None, :]
+    m = (c <= r) & ((c > r - window) if window else True)
+    qt = torch.from_numpy(q).permute(0, 2, 1, 3)
+    kt = torch.from_numpy(k).permute(0, 2, 1, 3).repeat_interleave(H // Hk, dim=1)
+    vt = torch.from_numpy(v).permute(0, 2, 1, 3).repeat_interleave(H // Hk, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(m),
+                                                           scale=scale)
+    assert np.allclose(O, ref.permute(0, 2, 1, 3).numpy(), atol=1e-13)
+    if window == 0:
+        ref2 = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True,
+                                                                scale=scale)
+        assert np.allclose(O, ref2.permute(0, 2, 1, 3).numpy(), atol=1e-13)
+    for h in range(H):
+        w = np.exp(st[0, h, :, :n] - L[0, h][None, :])
+        assert np.max(np.abs(w.sum(axis=0) - 1.0)) < 1e-12
+    # a key tile wholly after the row (causal) has no weight
+    assert np.all(st[0, 0, 4, :8] == -np.inf)

@@ -185,3 +185,28 @@ def test_lists_are_ascending_compactions():
                 c = L["q_cnt"][b, h, j]
                 assert list(L["q_idx"][b, h, j, :c]) == [i for i in range(5) if m[b, h, i, j]]
                 assert np.all(L["q_idx"][b, h, j, c:] == -1)
+
+
+def test_structurally_empty_tiles_brute_force():
+    """A tile is empty iff no (row, key) pair in it attends (checked pair by pair)."""
+    n, bq, bk = 50, 8, 16
+    for causal, window in ((True, 0), (True, 9), (True, 40)):
+        e = M.structurally_empty(-(-n // bq), -(-n // bk), n, bq, bk, causal, window)
+        for i in range(e.shape[0]):
+            for j in range(e.shape[1]):
+                rows = range(i * bq, min(n, (i + 1) * bq))
+                cols = range(j * bk, min(n, (j + 1) * bk))
+                some = any(c <= r and (window == 0 or c > r - window) for r in rows for c in cols)
+                assert e[i, j] == (not some), (causal, window, i, j)
+
+
+def test_causal_mask_keeps_nonempty_and_drops_empty_even_at_negl_zero():
+    n, b = 512, 64
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((1, n, 1, 16)) * 2
+    k = rng.standard_normal((1, n, 1, 16)) * 2
+    _, L, st = A.forward(q, k, k, 0.25, block_q=b, block_k=b, causal=True, window=150)
+    out = M.mask_from_stats(st.astype(np.float32), L.astype(np.float32), n, b, b, 0.0,
+                            causal=True, window=150)
+    empty = M.structurally_empty(n // b, n // b, n, b, b, True, 150)
+    assert np.all(out["mask"][0, 0][empty] == 0) and np.all(out["mask"][0, 0][~empty] == 1)
