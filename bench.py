@@ -182,17 +182,19 @@ def cpu_reference_sample(w, q, k, v, go, budget_s=15.0, max_tiles=256):
         qh = qn[0, :, h].astype(np.float64)
         kh = kn[0, :, hk].astype(np.float64)
         vh = vn[0, :, hk].astype(np.float64)
-        o_r, l_r, st_r = A.forward_head(qh, kh, vh, w.scale, rows=rows, block_k=w.block_k)
+        o_r, l_r, st_r = A.forward_head(qh, kh, vh, w.scale, rows=rows, block_k=w.block_k,
+                                        causal=w.causal, window=w.window)
         d = M.tile_weights(st_r.astype(np.float32), l_r.astype(np.float32), len(rows), w.block_q)
         act, _ = M.select_row(d[0], M.threshold(NEGL))
         tm = np.zeros((T_r, w.T_c), dtype=np.uint8)
         tm[i] = act
+        tm[M.structurally_empty(T_r, w.T_c, w.n, w.block_q, w.block_k, w.causal, w.window)] = 0
         o_full = np.zeros_like(qh)
         o_full[rows] = o_r
         lse_full = np.zeros(w.n)
         lse_full[rows] = l_r
         A.backward_head(qh, kh, vh, o_full, gn[0, :, h].astype(np.float64), lse_full, w.scale,
-                        tm, w.block_q, w.block_k, rows=rows)
+                        tm, w.block_q, w.block_k, rows=rows, causal=w.causal, window=w.window)
         done += 1
     el = time.perf_counter() - t0
     total_tiles = w.B * w.H * T_r
@@ -249,7 +251,7 @@ def run_ours(args):
     negl = args.negl
     # weak scaling: every rank runs its own independent problem (seed = rank)
     q, k, v, go = inputs.generate(w, seed=rank)
-    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window)
     T_r, T_c = _lib.tiles(shape)
     qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
     o = torch.empty_like(qd)
@@ -477,11 +479,13 @@ def run_all_configs(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     pk = _peaks()
-    for name in ("tiny_n256_d64", "clustered_n4096_d64", "gqa_n8192_d128",
-                 "video_n32760_d128", "long_n131072_d128"):
+    names = args.configs.split(",") if args.configs else [
+        "tiny_n256_d64", "clustered_n4096_d64", "gqa_n8192_d128", "video_n32760_d128",
+        "long_n131072_d128", "llm_causal_n16384_d128", "llm_window2048_n16384_d128"]
+    for name in names:
         w = inputs.WORKLOADS[name]
         q, k, v, go = inputs.generate(w, seed=0)
-        shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+        shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window)
         T_r, T_c = _lib.tiles(shape)
         qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
         o = torch.empty_like(qd)
@@ -563,6 +567,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--ref-tiles", type=int, default=256)
+    ap.add_argument("--configs", default="",
+                    help="comma-separated workloads for --all-configs (default: all)")
     ap.add_argument("--all-configs", action="store_true",
                     help="per-workload kernel times (not the contract line)")
     args = ap.parse_args()

@@ -27,7 +27,7 @@ EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("n", ctypes.c_int), ("H", ctypes.c_int),
                 ("Hk", ctypes.c_int), ("d", ctypes.c_int), ("block_q", ctypes.c_int),
-                ("block_k", ctypes.c_int)]
+                ("block_k", ctypes.c_int), ("causal", ctypes.c_int), ("window", ctypes.c_int)]
 
 
 class Lists(ctypes.Structure):
@@ -102,8 +102,8 @@ def _need(t, dtype, shape, name):
         raise ValueError(f"{name} must be contiguous")
 
 
-def make_shape(B, n, H, Hk, d, block_q, block_k) -> Shape:
-    return Shape(B, n, H, Hk, d, block_q, block_k)
+def make_shape(B, n, H, Hk, d, block_q, block_k, causal=0, window=0) -> Shape:
+    return Shape(B, n, H, Hk, d, block_q, block_k, int(causal), int(window))
 
 
 def tiles(shape: Shape):

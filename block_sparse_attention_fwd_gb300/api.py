@@ -10,6 +10,9 @@ builds the block-sparse mask from them before running the sparse backward
 (How It Works, Phase 2).  negl_prob = 0 records nothing and runs the dense
 backward (Key properties).  ``BL_VERBOSE=1`` prints mask density per head
 after each mask pass (README, Debugging, names the same kind of switch).
+``causal=True`` (optionally with ``window=W``) gives decoder attention, with
+the sliding windows of the "Introducing BackLite" post's Nanochat runs
+(Training Nanochat).
 
 PyTorch only allocates memory and supplies the stream; all arithmetic runs in
 libbl_attn.so.
@@ -31,10 +34,10 @@ def default_tiles(n: int, d: int):
 
 class _BLAttnFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, scale, negl_prob, block_q, block_k, tile_stats):
+    def forward(ctx, q, k, v, scale, negl_prob, block_q, block_k, tile_stats, causal, window):
         B, n, H, d = q.shape
         Hk = k.shape[2]
-        shape = _lib.make_shape(B, n, H, Hk, d, block_q, block_k)
+        shape = _lib.make_shape(B, n, H, Hk, d, block_q, block_k, causal, window)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
         stats = None
@@ -69,19 +72,22 @@ class _BLAttnFn(torch.autograd.Function):
         g_v = torch.empty_like(v)
         ws = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=q.device)
         _lib.attn_bwd(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, ws)
-        return g_q, g_k, g_v, None, None, None, None, None
+        return g_q, g_k, g_v, None, None, None, None, None, None, None
 
 
 class BLAttention(torch.nn.Module):
     """Attention whose backward skips the lightest tiles (negl_prob of the mass)."""
 
     def __init__(self, negl_prob: float = 0.05, block_q: int | None = None,
-                 block_k: int | None = None):
+                 block_k: int | None = None, causal: bool = False, window: int = 0):
         super().__init__()
         if not (0.0 <= negl_prob < 1.0):
             raise ValueError("negl_prob must lie in [0, 1)")
+        if window < 0 or (window and not causal):
+            raise ValueError("a sliding window needs causal=True")
         self.negl_prob = float(negl_prob)
         self.block_q, self.block_k = block_q, block_k
+        self.causal, self.window = bool(causal), int(window)
 
     def forward(self, query, key, value, scale=None, return_softmax_lse=False, tile_stats=None):
         d = query.shape[-1]
@@ -91,5 +97,6 @@ class BLAttention(torch.nn.Module):
         bq = self.block_q or bq
         bk = self.block_k or bk
         q, k, v = (t.contiguous() for t in (query, key, value))
-        o, lse = _BLAttnFn.apply(q, k, v, float(scale), self.negl_prob, bq, bk, tile_stats)
+        o, lse = _BLAttnFn.apply(q, k, v, float(scale), self.negl_prob, bq, bk, tile_stats,
+                                 int(self.causal), self.window)
         return (o, lse) if return_softmax_lse else o

@@ -19,9 +19,14 @@ bl_status check_shape(const bl_shape* s, bl::Shape* out) {
   if (s->d != 64 && s->d != 128) return BL_ERR_UNSUPPORTED;
   if ((s->block_q != 64 && s->block_q != 128) || (s->block_k != 64 && s->block_k != 128))
     return BL_ERR_UNSUPPORTED;
+  if (s->causal != 0 && s->causal != 1) return BL_ERR_INVALID_ARG;
+  if (s->window < 0 || (s->window > 0 && !s->causal)) return BL_ERR_INVALID_ARG;
+  if ((s->causal || s->window) && (s->block_q != 128 || s->block_k != 128))
+    return BL_ERR_UNSUPPORTED;
   bl::Shape sh;
   sh.B = s->B; sh.n = s->n; sh.H = s->H; sh.Hk = s->Hk; sh.d = s->d;
   sh.block_q = s->block_q; sh.block_k = s->block_k;
+  sh.causal = s->causal; sh.window = s->window;
   sh.T_r = (s->n + s->block_q - 1) / s->block_q;
   sh.T_c = (s->n + s->block_k - 1) / s->block_k;
   sh.n_pad = (int64_t)sh.T_r * s->block_q;

@@ -66,6 +66,7 @@ extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, c
   bl::Shape sh;
   sh.B = shape->B; sh.n = shape->n; sh.H = shape->H; sh.Hk = shape->Hk; sh.d = shape->d;
   sh.block_q = shape->block_q; sh.block_k = shape->block_k;
+  sh.causal = shape->causal; sh.window = shape->window;
   sh.T_r = (sh.n + sh.block_q - 1) / sh.block_q;
   sh.T_c = (sh.n + sh.block_k - 1) / sh.block_k;
   sh.n_pad = (int64_t)sh.T_r * sh.block_q;

@@ -39,6 +39,10 @@
 // Registers: the block starts at 128 per thread; warps 0-3 give some back
 // (setmaxnreg.dec to 64) so the drain warpgroup can hold a whole 128-column
 // dQ row (setmaxnreg.inc to 192): 128*64 + 256*128 + 128*192 = 65536.
+// Causal and sliding-window attention ("Introducing BackLite", Training
+// Nanochat): P^T entries of (key, query) pairs that do not attend are 0, so
+// they add nothing to any gradient; the mask never keeps a tile without an
+// attending pair and, without lists, the walk skips such tiles.
 // All hand-offs are mbarriers; every wait is bounded (tc.cuh).
 #include "common.cuh"
 #include "kernels.h"
@@ -127,6 +131,7 @@ struct Walk {
         corrupt = true;
         continue;
       }
+      if (!q_idx && tile_empty(*sh, i, j)) continue;   // dense walk: nothing attends
       return true;
     }
   }
@@ -134,7 +139,8 @@ struct Walk {
 
 __device__ __forceinline__ bool failed(const int* f) { return *(volatile const int*)f != 0; }
 
-template <int D>
+// MASKED: causal / sliding-window element masks are compiled in.
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -387,6 +393,12 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       fence_after_sync();
       const float* sl = reinterpret_cast<const float*>(sm + C::OFF_L) + s * 128 + half * 64;
       const float* sd = reinterpret_cast<const float*>(sm + C::OFF_D) + s * 128 + half * 64;
+      // this key row attends query columns q_lo..q_hi of the warpgroup's 64:
+      // query >= key (causal) and query < key + window (window)
+      const int kq = j * 128 + r - walk.i * 128 - half * 64;
+      const int q_lo = MASKED && sh.causal ? kq : 0;
+      const int q_hi = MASKED && sh.window ? kq + sh.window - 1 : 63;
+      const bool diag = MASKED && __any_sync(0xffffffffu, q_lo > 0 || q_hi < 63);
       float pf[64];
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {    // 32 query columns per pass
@@ -404,6 +416,14 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             pf[pass * 32 + c] =
                 key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
           }
+        }
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (pass * 32 + c < q_lo || pass * 32 + c > q_hi) pf[pass * 32 + c] = 0.f;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
           pk[2 * c4] = pack_bf16(pf[pass * 32 + 4 * c4], pf[pass * 32 + 4 * c4 + 1]);
           pk[2 * c4 + 1] = pack_bf16(pf[pass * 32 + 4 * c4 + 2], pf[pass * 32 + 4 * c4 + 3]);
         }
@@ -540,7 +560,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
   if (warp == 1) tmem_free(tmem, C::T_COLS);
 }
 
-template <int D>
+template <int D, bool MASKED>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, const void* g_o,
                      const float* lse, const float* Dv, const int32_t* q_idx,
                      const int32_t* q_cnt, void* g_k, void* g_v, float* dq_acc, int32_t* status,
@@ -556,7 +576,7 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
       !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
-  auto kern = bwd_tc_kernel<D>;
+  auto kern = bwd_tc_kernel<D, MASKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(sh.T_c, sh.Hk, sh.B);
@@ -575,9 +595,16 @@ cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const v
                           const void* g_o, const float* lse, const float* Dv,
                           const int32_t* q_idx, const int32_t* q_cnt, void* g_k, void* g_v,
                           float* dq_acc, int32_t* status, float scale, cudaStream_t st) {
+  const bool masked = sh.causal || sh.window;
   if (sh.d == 128)
-    return launch_t<128>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc, status, scale, st);
-  return launch_t<64>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc, status, scale, st);
+    return masked ? launch_t<128, true>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
+                                        status, scale, st)
+                  : launch_t<128, false>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
+                                         status, scale, st);
+  return masked ? launch_t<64, true>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
+                                     status, scale, st)
+                : launch_t<64, false>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
+                                      status, scale, st);
 }
 
 }  // namespace bl

@@ -14,7 +14,33 @@ struct Shape {
   int B, n, H, Hk, d, block_q, block_k;
   int T_r, T_c;
   int64_t n_pad;  // T_r * block_q
+  int causal, window;
 };
+
+// Key tiles [lo, hi] of query tile i that hold at least one attending
+// (query, key) pair under the causal / sliding-window structure: causal keeps
+// keys c <= r, so the last such tile holds the tile's last row; a window W
+// keeps keys c >= r - W + 1, so the first holds key r0 - W + 1 of the tile's
+// first row r0.  Without structure the range is every key tile.
+__host__ __device__ __forceinline__ void key_tile_range(const Shape& sh, int i, int& lo, int& hi) {
+  lo = 0;
+  hi = sh.T_c - 1;
+  const int r0 = i * sh.block_q;
+  const int r1 = min(sh.n, (i + 1) * sh.block_q) - 1;
+  if (sh.causal) hi = min(hi, r1 / sh.block_k);
+  if (sh.window) {
+    const int x = r0 - sh.window + 1;
+    if (x > 0) lo = x / sh.block_k;
+  }
+}
+
+// True when no (query, key) pair of tile (i, j) attends.
+__host__ __device__ __forceinline__ bool tile_empty(const Shape& sh, int i, int j) {
+  if (!sh.causal && !sh.window) return false;
+  int lo, hi;
+  key_tile_range(sh, i, lo, hi);
+  return j < lo || j > hi;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

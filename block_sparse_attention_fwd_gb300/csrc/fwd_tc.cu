@@ -24,6 +24,12 @@
 //   warps 4-7  softmax warpgroup of tile A, warps 8-11 of tile B; thread =
 //              query row: S row from TMEM, tile statistic (coalesced 512 B
 //              per key tile), P back into TMEM; at the end O = acc / l, LSE.
+// Causal and sliding-window attention (the BackLite blog's Nanochat runs,
+// "Introducing BackLite", Training Nanochat): a pair visits only the key
+// tiles [lo, hi] that hold an attending pair for one of its two query
+// tiles; scores of keys a row does not attend are -inf before the max, and
+// the statistics of the key tiles outside [lo, hi] are written as -inf.  The
+// heaviest pairs (latest query tiles) are launched first.
 // Every mbarrier wait is bounded (tc.cuh).
 #include "common.cuh"
 #include "kernels.h"
@@ -72,11 +78,20 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   __shared__ int s_fail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // under causal structure later pairs visit more key tiles: start them first
+  const int pair = (sh.causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (sh.H / sh.Hk);
   const int Tc = sh.T_c;
   // the second tile of the last pair may lie wholly past the last query tile
   const int ntile = min(2, sh.T_r - 2 * pair);
+  // key tiles [j_lo, j_hi] hold an attending pair for tile A or tile B; the
+  // rings and barrier phases count visits jj = j - j_lo
+  int j_lo, j_hi, lo_b, hi_b;
+  key_tile_range(sh, 2 * pair, j_lo, j_hi);
+  key_tile_range(sh, 2 * pair + ntile - 1, lo_b, hi_b);
+  j_hi = hi_b;
+  const int nj = j_hi - j_lo + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q, 1);
@@ -114,27 +129,27 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
         for (int c = 0; c < C::CHK; ++c)
           tma_load_4d(sm + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK, &tm_q, &bars.q, c * 64,
                       h, (2 * pair + t) * 128, b);
-      auto load_v = [&](int jv) -> bool {
+      auto load_v = [&](int jv) -> bool {   // jv counts visits
         const int sv = jv % C::NV;
         if (!mbar_wait(&bars.v_empty[sv], ((jv / C::NV) & 1) ^ 1)) return false;
         mbar_expect_tx(&bars.v_full[sv], C::TILE_BYTES);
         for (int c = 0; c < C::CHK; ++c)
           tma_load_4d(sm + C::OFF_V + sv * C::TILE_BYTES + c * C::CHUNK, &tm_v, &bars.v_full[sv],
-                      c * 64, hk, jv * 128, b);
+                      c * 64, hk, (j_lo + jv) * 128, b);
         return true;
       };
       bool ok = true;
-      for (int j = 0; ok && j <= Tc; ++j) {
-        if (j < Tc) {
-          const int sk = j % C::NK;
-          ok = !failed(&s_fail) && mbar_wait(&bars.k_empty[sk], ((j / C::NK) & 1) ^ 1);
+      for (int jj = 0; ok && jj <= nj; ++jj) {
+        if (jj < nj) {
+          const int sk = jj % C::NK;
+          ok = !failed(&s_fail) && mbar_wait(&bars.k_empty[sk], ((jj / C::NK) & 1) ^ 1);
           if (!ok) break;
           mbar_expect_tx(&bars.k_full[sk], C::TILE_BYTES);
           for (int c = 0; c < C::CHK; ++c)
             tma_load_4d(sm + C::OFF_K + sk * C::TILE_BYTES + c * C::CHUNK, &tm_k,
-                        &bars.k_full[sk], c * 64, hk, j * 128, b);
+                        &bars.k_full[sk], c * 64, hk, (j_lo + jj) * 128, b);
         }
-        if (j >= 1) ok = load_v(j - 1);   // V stays one key tile behind K
+        if (jj >= 1) ok = load_v(jj - 1);   // V stays one key tile behind K
       }
       if (!ok) fail();
     }
@@ -143,8 +158,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     if (lane == 0) {
       const uint32_t sQ = saddr(sm + C::OFF_Q), sK = saddr(sm + C::OFF_K);
       const uint32_t sV = saddr(sm + C::OFF_V);
-      auto issue_s = [&](int t, int j) {   // S_t(j) = Q_t K_j^T into S_t
-        const uint32_t qb = sQ + t * C::TILE_BYTES, kb = sK + (j % C::NK) * C::TILE_BYTES;
+      auto issue_s = [&](int t, int jj) {   // S_t = Q_t K^T of visit jj into S_t
+        const uint32_t qb = sQ + t * C::TILE_BYTES, kb = sK + (jj % C::NK) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
@@ -153,13 +168,13 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
         }
         mma_commit(&bars.s_full[t]);
       };
-      auto issue_pv = [&](int t, int j) {  // O_t += P_t(j) V_j, P_t read from TMEM
-        const uint32_t vb = sV + (j % C::NV) * C::TILE_BYTES;
+      auto issue_pv = [&](int t, int jj) {  // O_t += P_t V of visit jj, P_t read from TMEM
+        const uint32_t vb = sV + (jj % C::NV) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + C::T_O + t * D, tmem + C::T_S + t * 128 + kk * 8,
                  sdesc_sw128(vb + kk * 2048, C::CHUNK, 1024), C::ID_O,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+                 (jj > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(&bars.q, 0) && mbar_wait(&bars.k_full[0], 0);
       if (ok) {
@@ -167,23 +182,23 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
         for (int t = 0; t < ntile; ++t) issue_s(t, 0);
         mma_commit(&bars.k_empty[0]);
       }
-      for (int j = 0; ok && j < Tc; ++j) {
-        const bool more = j + 1 < Tc;
+      for (int jj = 0; ok && jj < nj; ++jj) {
+        const bool more = jj + 1 < nj;
         if (more)
           ok = !failed(&s_fail) &&
-               mbar_wait(&bars.k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1);
-        if (ok) ok = mbar_wait(&bars.v_full[j % C::NV], (j / C::NV) & 1);
+               mbar_wait(&bars.k_full[(jj + 1) % C::NK], ((jj + 1) / C::NK) & 1);
+        if (ok) ok = mbar_wait(&bars.v_full[jj % C::NV], (jj / C::NV) & 1);
         for (int t = 0; ok && t < ntile; ++t) {
-          ok = mbar_wait(&bars.p_ready[t], j & 1);
+          ok = mbar_wait(&bars.p_ready[t], jj & 1);
           if (!ok) break;
           fence_after_sync();
-          issue_pv(t, j);
-          // S_t(j+1) overwrites P_t(j) in TMEM; it is queued after PV_t(j)
-          if (more) issue_s(t, j + 1);
+          issue_pv(t, jj);
+          // S_t(jj+1) overwrites P_t(jj) in TMEM; it is queued after PV_t(jj)
+          if (more) issue_s(t, jj + 1);
         }
         if (!ok) break;
-        mma_commit(&bars.v_empty[j % C::NV]);
-        if (more) mma_commit(&bars.k_empty[(j + 1) % C::NK]);
+        mma_commit(&bars.v_empty[jj % C::NV]);
+        if (more) mma_commit(&bars.k_empty[(jj + 1) % C::NK]);
       }
       if (!ok) fail();
       for (int t = 0; t < 2; ++t) mma_commit(&bars.o_done[t]);
@@ -202,8 +217,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     float* st_row = stats ? stats + bh * sh.T_c * sh.n_pad + row : nullptr;
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = valid_tile;
-    for (int j = 0; ok && j < Tc; ++j) {
-      ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.s_full[t], j & 1));
+    for (int jj = 0; ok && jj < nj; ++jj) {
+      const int j = j_lo + jj;
+      ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.s_full[t], jj & 1));
       if (!ok) break;
       fence_after_sync();
       uint32_t x[128];
@@ -211,11 +227,15 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       for (int c = 0; c < 4; ++c)
         tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
       tmem_ld_wait();
-      const int valid = sh.n - j * 128;            // keys of this tile that exist
-      if (valid < 128) {
+      // this row attends keys c_lo..c_hi of the tile: keys that exist, c <= row
+      // (causal), c > row - window (window)
+      int c_hi = sh.n - j * 128 - 1, c_lo = 0;
+      if (sh.causal) c_hi = min(c_hi, row - j * 128);
+      if (sh.window) c_lo = row - sh.window + 1 - j * 128;
+      if (__any_sync(0xffffffffu, c_hi < 127 || c_lo > 0)) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c >= valid) x[c] = __float_as_uint(-INFINITY);
+          if (c > c_hi || c < c_lo) x[c] = __float_as_uint(-INFINITY);
       }
       // max over the raw scores (the scale is positive), in base-2 units
       float mr = __uint_as_float(x[0]);
@@ -225,12 +245,14 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       const bool grow = mt > m_ref + C::kRescale;
       const float m_new = grow ? mt : m_ref;
       const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
+      // a row that has attended no key yet keeps m = -inf: its p are 0
+      const float m_sub = m_new == -INFINITY ? 0.f : m_new;
       float ts = 0.f;
       // p = 2^(x s log2 e - m); bf16 pairs packed in place (entry c from 2c, 2c+1)
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), scale_log2, -m_new));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), scale_log2, -m_new));
+        const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), scale_log2, -m_sub));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), scale_log2, -m_sub));
         ts += p0 + p1;
         x[c] = pack_bf16(p0, p1);
       }
@@ -241,9 +263,10 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
         st_row[(int64_t)j * sh.n_pad] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
       l_run = l_run * alpha + ts;
       m_ref = m_new;
-      // rescale O in TMEM (rare).  S_t(j) has completed, hence so has PV_t(j-1):
-      // the MMA issuer queues S_t(j) behind it; PV_t(j) waits for p_ready.
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+      // rescale O in TMEM (rare).  S_t(jj) has completed, hence so has
+      // PV_t(jj-1): the MMA issuer queues S_t(jj) behind it; PV_t(jj) waits
+      // for p_ready.
+      if (jj > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
           uint32_t ov[16];
@@ -260,6 +283,11 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     }
     if (valid_tile) {
       if (!ok && lane == 0) fail();
+      // key tiles this pair never visits carry no weight for this row
+      if (st_row) {
+        for (int j = 0; j < j_lo; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
+        for (int j = j_hi + 1; j < Tc; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
+      }
       // epilogue: O = acc / l, LSE = ln 2 (m + log2 l), once the last PV landed
       const bool done = __all_sync(0xffffffffu, ok && mbar_wait(&bars.o_done[t], 0));
       fence_after_sync();

@@ -93,6 +93,10 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
     lrow[e] = valid[e] ? lse[bh * sh.n + r0 + e] : 0.f;
   }
   const float* st = stats + bh * sh.T_c * sh.n_pad + r0;
+  // key tiles with no attending pair (causal / window) have statistic -inf:
+  // their d is -inf without a load, and they are never kept
+  int k_lo, k_hi;
+  key_tile_range(sh, i, k_lo, k_hi);
   constexpr int NW = kMaskThreads / 32;
   constexpr int UNR = 4;   // key tiles in flight per warp
   for (int j0 = warp; j0 < Tc; j0 += NW * UNR) {
@@ -101,6 +105,11 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
     for (int u = 0; u < UNR; ++u) {
       const int j = j0 + u * NW;
       if (j >= Tc) continue;
+      if (j < k_lo || j > k_hi) {
+#pragma unroll
+        for (int e = 0; e < RPL; ++e) vals[u][e] = -INFINITY;
+        continue;
+      }
       if constexpr (RPL == 4) {
         float4 x = *reinterpret_cast<const float4*>(st + (int64_t)j * sh.n_pad);
         vals[u][0] = x.x; vals[u][1] = x.y; vals[u][2] = x.z; vals[u][3] = x.w;
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
   int cnt_run = 0;
   for (int j0 = 0; j0 < Tc; j0 += kMaskThreads) {
     int j = j0 + tid;
-    int f = (j < Tc) ? s_act[j] : 0;
+    int f = (j < Tc && j >= k_lo && j <= k_hi) ? s_act[j] : 0;
     if (j < Tc) mrow[j] = (uint8_t)f;
     unsigned bal = __ballot_sync(0xffffffffu, f);
     int wpos = __popc(bal & ((1u << lane) - 1u));

@@ -20,11 +20,13 @@ Recipe (one numpy PCG64 stream per call, seed 0 unless stated):
 Values are drawn in fp32 and rounded to bf16 (round to nearest even); the
 oracle reads exactly these bf16 values, widened to fp64.
 
-The five workloads mirror the shapes that the BackLite pages motivate: the
+The workloads mirror the shapes that the BackLite pages motivate: the
 long-sequence video DiT regime ("Introducing BackLite", Introduction: 32k
 tokens for a 5 s 480p Wan 2.1 video) and long-context LLM training (same
-section: 128k contexts), plus two small cases and a GQA case
-("BackLite" README, Forward signature: key/value carry ``heads_k`` heads).
+section: 128k contexts), causal and sliding-window LLM training (same
+post, Training Nanochat: windows of 1024 and 2048), plus two small cases and
+a GQA case ("BackLite" README, Forward signature: key/value carry
+``heads_k`` heads).
 """
 from __future__ import annotations
 
@@ -52,6 +54,8 @@ class Workload:
     clusters: int = 0
     grid: tuple = ()               # (T, Y, X) for kind == "grid"
     patch: tuple = ()              # (pt, py, px) for kind == "grid"
+    causal: bool = False           # query r attends keys c <= r
+    window: int = 0                # with causal: keys r - window < c <= r
 
     @property
     def scale(self) -> float:
@@ -65,12 +69,23 @@ class Workload:
     def T_c(self) -> int:
         return -(-self.n // self.block_k)
 
+    def attending_pairs(self) -> int:
+        """(query, key) pairs per head that attend under causal / window."""
+        n = self.n
+        if not self.causal:
+            return n * n
+        if not self.window or self.window >= n:
+            return n * (n + 1) // 2
+        w = self.window
+        return w * (w + 1) // 2 + (n - w) * w
+
     def dense_bwd_flop(self) -> float:
-        """10*B*H*n^2*d: the five n x n x d contractions of the dense backward."""
-        return 10.0 * self.B * self.H * self.n * self.n * self.d
+        """10*B*H*pairs*d: the five contractions of the dense backward over the
+        (query, key) pairs that attend (n^2 without causal structure)."""
+        return 10.0 * self.B * self.H * self.attending_pairs() * self.d
 
     def dense_fwd_flop(self) -> float:
-        return 4.0 * self.B * self.H * self.n * self.n * self.d
+        return 4.0 * self.B * self.H * self.attending_pairs() * self.d
 
 
 WORKLOADS = {
@@ -98,15 +113,27 @@ WORKLOADS = {
                                   d=128, block_q=128, block_k=128,
                                   negl_probs=(0.05,), kind="runs", alpha=3.0,
                                   run=128, clusters=256),
+    # decoder-style LLM training: causal, and causal with the 1024 / 2048
+    # sliding windows of the BackLite blog's Nanochat runs
+    "llm_causal_n16384_d128": Workload("llm_causal_n16384_d128", B=1, n=16384, H=32, Hk=8,
+                                       d=128, block_q=128, block_k=128,
+                                       negl_probs=(0.05,), kind="runs", alpha=3.0,
+                                       run=64, clusters=64, causal=True),
+    "llm_window2048_n16384_d128": Workload("llm_window2048_n16384_d128", B=1, n=16384, H=32,
+                                           Hk=8, d=128, block_q=128, block_k=128,
+                                           negl_probs=(0.05,), kind="runs", alpha=3.0,
+                                           run=64, clusters=64, causal=True, window=2048),
 }
 
 
 def custom(name="custom", *, B, n, H, Hk, d, block_q=128, block_k=128,
-           kind="runs", alpha=3.0, run=64, clusters=16, negl_probs=(0.05,)):
+           kind="runs", alpha=3.0, run=64, clusters=16, negl_probs=(0.05,),
+           causal=False, window=0):
     """A workload of arbitrary shape with the 1-D clustered (or iid) recipe."""
     return Workload(name, B=B, n=n, H=H, Hk=Hk, d=d, block_q=block_q,
                     block_k=block_k, negl_probs=tuple(negl_probs), kind=kind,
-                    alpha=alpha, run=run, clusters=clusters)
+                    alpha=alpha, run=run, clusters=clusters, causal=causal,
+                    window=window)
 
 
 def cluster_of_token(w: Workload) -> np.ndarray:

@@ -54,10 +54,18 @@ typedef enum {
 /* Problem shape.  d in {64, 128}; block_q, block_k in {64, 128}; H % Hk == 0;
  * n >= 1.  One shape describes the forward, the mask and the backward: the
  * statistics, the mask and the backward all use the same block_q x block_k
- * tiles. */
+ * tiles.
+ *   causal  0: every query attends to every key; 1: query r attends to keys
+ *           c <= r.
+ *   window  0: no limit; W > 0 (needs causal = 1): query r attends to keys
+ *           r - W < c <= r, the sliding windows the BackLite blog trains
+ *           Nanochat with ("Introducing BackLite", Training Nanochat).
+ * causal/window need 128 x 128 tiles.  A tile with no attending (query, key)
+ * pair has tile statistic -inf and is never kept by the mask. */
 typedef struct {
   int B, n, H, Hk, d;
   int block_q, block_k;
+  int causal, window;
 } bl_shape;
 
 /* Block-sparse tile lists of one backward, all device memory.

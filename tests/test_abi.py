@@ -118,3 +118,15 @@ def test_combine_rejects_bad_arguments(lib):
     assert lib.bl_lse_combine(33, 1, 8, 1, 64, ok, ok, ok, ok, None) == 1
     assert lib.bl_lse_combine(2, 1, 8, 1, 96, ok, ok, ok, ok, None) == 2
     assert lib.bl_lse_combine(2, 1, 8, 1, 64, None, ok, ok, ok, None) == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(causal=0, window=64, block_q=128, block_k=128), 1),     # a window needs causal
+    (dict(causal=2, block_q=128, block_k=128), 1),
+    (dict(causal=1, window=-1, block_q=128, block_k=128), 1),
+    (dict(causal=1), 2),                                           # 64 x 64 tiles
+    (dict(causal=1, block_q=128, block_k=64), 2)])
+def test_causal_shape_checks(lib, kw, code):
+    s = _shape(**kw)
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.bl_attn_fwd(ctypes.byref(s), fake, fake, fake, 0.125, fake, fake, None, None) == code

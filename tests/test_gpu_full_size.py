@@ -54,7 +54,7 @@ def _oracle_mask_head(w, orc, negl):
 
 def _gpu_forward(w, q, k, v):
     from block_sparse_attention_fwd_gb300 import _lib
-    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window)
     return (shape,) + U.gpu_forward(shape, q, k, v, w.scale)
 
 

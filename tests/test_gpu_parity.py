@@ -43,7 +43,7 @@ def test_hot_path_matches_oracle(case):
     from block_sparse_attention_fwd_gb300 import _lib
     q, k, v, go = inputs.generate(w, seed=0)
     scale = w.scale
-    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window)
 
     # ---- forward + statistics
     qd, kd, vd, o, lse, stats = U.gpu_forward(shape, q, k, v, scale)
@@ -128,7 +128,7 @@ def test_corrupt_list_entry_is_reported_not_faulted(tile, d):
     from block_sparse_attention_fwd_gb300 import _lib
     w = inputs.custom("corrupt", B=1, n=4 * tile, H=1, Hk=1, d=d, block_q=tile, block_k=tile)
     q, k, v, go = inputs.generate(w)
-    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window)
     qd, kd, vd, o, lse, stats = U.gpu_forward(shape, q, k, v, w.scale)
     lists = U.gpu_mask(shape, stats, lse, 0.05)
     lists["q_idx"][0, 0, 0, 0] = 99          # out of range: T_r = 4

@@ -46,7 +46,7 @@ def test_noalloc_matches_workspace_backward_twice(tile, d, negl):
                       run=40, clusters=6, alpha=3.0)
     q, k, v, go = inputs.generate(w, seed=3)
     dev = torch.device("cuda")
-    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window)
     assert _lib.bwd_workspace_bytes(shape) <= 32 * 1024 * 1024
     qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
     o = torch.empty_like(qd)
