@@ -18,15 +18,20 @@
 //                       of dV += P^T dO
 //   R_dP [128,256)      dP^T; after the softmax, the dQ tile dS K
 //   dV   [256,256+d)    dK [256+d,256+2d)
-// The order in which one thread issues the MMAs makes every reuse safe: the
-// tensor core runs them in issue order, so S^T of the next tile (into R_S) is
-// queued behind dV (which reads P^T from R_S) and dQ (which reads dS^T from
-// shared memory), and dP^T of the next tile is issued only after the dQ
-// tile has been drained from R_dP.
+// Per tile the issuer queues dV as soon as the softmax has written P^T
+// (first phase) and the next tile's S^T right behind it, so S^T runs while
+// the softmax forms dS^T (second phase); then dK and dQ once dS^T is in
+// shared memory, and the next tile's dP^T once the dQ tile has been drained
+// from R_dP.  The tensor core runs them in issue order, which makes every
+// reuse safe: S^T of the next tile (into R_S) is queued behind dV, which
+// reads P^T from R_S, and dS^T is rewritten only after the next dP^T, hence
+// after dK and dQ, have completed.
 // Warp roles (16 warps):
-//   warp 0      TMA producer: K_j, V_j once; then Q_i and dO_i tiles into a
-//               3-slot ring (4-D tensor maps, 128-byte swizzle, rows past n
-//               read as 0), plus the tile's LSE and D rows.
+//   warp 0      TMA producer: K_j, V_j once; then Q_i into two alternating
+//               slots and dO_i into a third (4-D tensor maps, 128-byte
+//               swizzle, rows past n read as 0), plus the tile's LSE and D
+//               rows; dO's slot frees once dV has read it, so the next dO
+//               loads while dK, S^T and dQ run.
 //   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2-3   at start: copy this CTA's tile lists into shared memory.
 //   warps 4-7   softmax, query columns 0-63; warps 8-11 columns 64-127.
@@ -56,7 +61,7 @@ using namespace tc;
 
 template <int D>
 struct Cfg {
-  static constexpr int NS = 3;                    // ring slots, one Q or dO tile each
+  static constexpr int NS = 3;                    // tile slots: Q_t in slot t % 2, dO in slot 2
   static constexpr int CHK = D / 64;              // 64-element chunks along d
   static constexpr int CHUNK = 128 * 128;         // [128 rows][128 B]
   static constexpr int TILE = CHUNK * CHK;        // one 128 x d bf16 tile
@@ -83,8 +88,17 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t kv, full[3], empty[3], s_full, dp_full, p_ready, dq_ready, dq_free, acc;
+  uint64_t kv, full[3], empty[3], s_full, dp_full, p1_ready, p2_ready, dq_ready, dq_free, acc;
 };
+
+// Load x = 2t brings Q_t, x = 2t + 1 brings dO_t.  Q_t alternates between
+// slots 0 and 1 (its last reader, dK_t, frees it); every dO uses slot 2,
+// which frees as soon as dV_t (its last reader) completes, so the next dO
+// loads while dK_t, S^T and dQ run.
+__device__ __forceinline__ int slot_of(int x) { return (x & 1) ? 2 : ((x >> 1) & 1); }
+__device__ __forceinline__ uint32_t phase_of(int x) {
+  return (uint32_t)(((x & 1) ? (x >> 1) : (x >> 2)) & 1);
+}
 
 // Iterates the kept query tiles of key tile j over the heads of one GQA group,
 // identically in every role.  Reads the lists from shared memory when they
@@ -171,7 +185,8 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_ready, 256);
+    mbar_init(&bars.p1_ready, 256);
+    mbar_init(&bars.p2_ready, 256);
     mbar_init(&bars.dq_ready, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.acc, 1);
@@ -246,7 +261,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       const int64_t bh = (int64_t)b * sh.H + walk.h;
       const int r0 = walk.i * 128;
       for (int which = 0; which < 2 && ok; ++which, ++x) {
-        const int s = x % C::NS;
+        const int s = slot_of(x);
         float lv[4], dv[4];
         if (which == 0) {   // this tile's LSE and D travel with its Q slot
 #pragma unroll
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             dv[e] = in ? Dv[bh * sh.n + r] : 0.f;
           }
         }
-        ok = !failed(&s_fail) && mbar_wait(&bars.empty[s], ((x / C::NS) & 1) ^ 1);
+        ok = !failed(&s_fail) && mbar_wait(&bars.empty[s], phase_of(x) ^ 1);
         if (!ok) break;
         if (lane == 0) {
           mbar_expect_tx(&bars.full[s], C::TILE);
@@ -284,7 +299,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     if (lane == 0) {
       const uint32_t sK = saddr(sm + C::OFF_K), sV = saddr(sm + C::OFF_V);
       const uint32_t sR = saddr(sm + C::OFF_RING), sDS = saddr(sm + C::OFF_DS);
-      auto slot_addr = [&](int xx) { return sR + (xx % C::NS) * C::TILE; };
+      auto slot_addr = [&](int xx) { return sR + slot_of(xx) * C::TILE; };
       auto issue_s = [&](int t) {      // S^T = K Q_t^T  -> R_S
         const uint32_t qb = slot_addr(2 * t);
 #pragma unroll
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         mma_commit(&bars.dp_full);
       };
       auto wait_slot = [&](int xx) {
-        return mbar_wait(&bars.full[xx % C::NS], (xx / C::NS) & 1);
+        return mbar_wait(&bars.full[slot_of(xx)], phase_of(xx));
       };
       bool ok = mbar_wait(&bars.kv, 0);
       int t = 0;
@@ -324,8 +339,9 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         }
       }
       while (ok && have) {
-        // gradients of tile t once its softmax has written P^T and dS^T
-        ok = !failed(&s_fail) && mbar_wait(&bars.p_ready, t & 1);
+        // dV_t as soon as the first softmax phase has written P^T; it runs
+        // while the second phase forms dS^T
+        ok = !failed(&s_fail) && mbar_wait(&bars.p1_ready, t & 1);
         if (!ok) break;
         fence_after_sync();
         const uint32_t qb = slot_addr(2 * t), gb = slot_addr(2 * t + 1);
@@ -335,17 +351,10 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
           mma_ts(tmem + C::T_DV, tmem + pcol, sdesc_sw128(gb + kk * 2048, C::CHUNK, 1024),
                  C::ID_G, (t > 0 || kk > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)        // dK += dS^T Q
-          mma_ss(tmem + C::T_DK,
-                 sdesc_sw128(sDS + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024),
-                 sdesc_sw128(qb + kk * 2048, C::CHUNK, 1024), C::ID_G,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.empty[(2 * t) % C::NS]);
-        mma_commit(&bars.empty[(2 * t + 1) % C::NS]);
-        // S^T of the next tile goes ahead of dQ so that the first softmax phase
-        // of that tile overlaps the dQ product and its drain.  It is queued
-        // behind dV, which read P^T from R_S.
+        mma_commit(&bars.empty[2]);           // dO_t's slot: dP^T and dV have read it
+        // S^T of the next tile right behind dV (which read P^T from R_S): it
+        // runs while the softmax forms dS^T, so the first softmax phase of the
+        // next tile can start as soon as the second phase of this one ends
         have = walk.next();
         if (have) {
           ok = wait_slot(2 * (t + 1));
@@ -353,6 +362,17 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
           fence_after_sync();
           issue_s(t + 1);
         }
+        // dK_t once dS^T is in shared memory
+        ok = mbar_wait(&bars.p2_ready, t & 1);
+        if (!ok) break;
+        fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)        // dK += dS^T Q
+          mma_ss(tmem + C::T_DK,
+                 sdesc_sw128(sDS + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024),
+                 sdesc_sw128(qb + kk * 2048, C::CHUNK, 1024), C::ID_G,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.empty[t & 1]);       // Q_t's slot
         // dQ = dS K into R_dP (dP^T was consumed by the softmax)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -384,10 +404,10 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     int t = 0;
     bool ok = true;
     while (ok && walk.next()) {
-      const int s = (2 * t) % C::NS;
+      const int s = t & 1;                      // Q_t's slot: its LSE and D rows
       // phase 1: P^T from S^T (needs only S^T), written back over S^T
       ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
-                                       mbar_wait(&bars.full[s], ((2 * t) / C::NS) & 1) &&
+                                       mbar_wait(&bars.full[s], (t >> 1) & 1) &&
                                        mbar_wait(&bars.s_full, t & 1));
       if (!ok) break;
       fence_after_sync();
@@ -401,70 +421,74 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       const bool diag = MASKED && __any_sync(0xffffffffu, q_lo > 0 || q_hi < 63);
       float pf[64];
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {    // 32 query columns per pass
-        uint32_t sv[32];
-        tmem_ld32(lane_base + C::T_S + half * 64 + pass * 32, sv);
-        tmem_ld_wait();
+      for (int h2 = 0; h2 < 2; ++h2) {          // 32 query columns -> 16 packed
         uint32_t pk[16];
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 l4 = reinterpret_cast<const float4*>(sl + pass * 32)[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int sub = 0; sub < 2; ++sub) {     // 16 query columns per load
+          const int c0 = h2 * 32 + sub * 16;
+          uint32_t sv[16];
+          tmem_ld16(lane_base + C::T_S + half * 64 + c0, sv);
+          tmem_ld_wait();
 #pragma unroll
-          for (int y = 0; y < 4; ++y) {
-            const int c = 4 * c4 + y;
-            pf[pass * 32 + c] =
-                key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 l4 = reinterpret_cast<const float4*>(sl + c0)[c4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+              const int c = 4 * c4 + y;
+              pf[c0 + c] =
+                  key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
+            }
           }
-        }
-        if (diag) {
+          if (diag) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (pass * 32 + c < q_lo || pass * 32 + c > q_hi) pf[pass * 32 + c] = 0.f;
-        }
+            for (int c = 0; c < 16; ++c)
+              if (c0 + c < q_lo || c0 + c > q_hi) pf[c0 + c] = 0.f;
+          }
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          pk[2 * c4] = pack_bf16(pf[pass * 32 + 4 * c4], pf[pass * 32 + 4 * c4 + 1]);
-          pk[2 * c4 + 1] = pack_bf16(pf[pass * 32 + 4 * c4 + 2], pf[pass * 32 + 4 * c4 + 3]);
+          for (int c2 = 0; c2 < 8; ++c2)
+            pk[sub * 8 + c2] = pack_bf16(pf[c0 + 2 * c2], pf[c0 + 2 * c2 + 1]);
         }
         // P^T pairs over this warpgroup's own S^T columns (already read)
-        tmem_st16(lane_base + C::T_S + half * 64 + pass * 16, pk);
+        tmem_st16(lane_base + C::T_S + half * 64 + h2 * 16, pk);
       }
+      tmem_st_wait();
+      fence_before_sync();
+      mbar_arrive(&bars.p1_ready);               // dV_t may read P^T now
       // phase 2: dS^T = P^T (dP^T - D) once dP^T has landed
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, t & 1));
       if (!ok) break;
       fence_after_sync();
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        uint32_t pv[32];
-        tmem_ld32(lane_base + C::T_DP + half * 64 + pass * 32, pv);
+      for (int pass = 0; pass < 4; ++pass) {    // 16 query columns per pass
+        uint32_t pv[16];
+        tmem_ld16(lane_base + C::T_DP + half * 64 + pass * 16, pv);
         tmem_ld_wait();
-        uint32_t dk[16];
+        uint32_t dk[8];
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = reinterpret_cast<const float4*>(sd + pass * 32)[c4];
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 d4 = reinterpret_cast<const float4*>(sd + pass * 16)[c4];
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float ds[4];
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
             const int c = 4 * c4 + y;
-            ds[y] = pf[pass * 32 + c] * (__uint_as_float(pv[c]) - dv[y]);
+            ds[y] = pf[pass * 16 + c] * (__uint_as_float(pv[c]) - dv[y]);
           }
           dk[2 * c4] = pack_bf16(ds[0], ds[1]);
           dk[2 * c4 + 1] = pack_bf16(ds[2], ds[3]);
         }
-        // dS^T, K-major [key][q] with the 128-byte swizzle, 4 x 16 B chunks
+        // dS^T, K-major [key][q] with the 128-byte swizzle, 2 x 16 B chunks
 #pragma unroll
-        for (int c16 = 0; c16 < 4; ++c16) {
-          const int chunk = pass * 4 + c16;
+        for (int c16 = 0; c16 < 2; ++c16) {
+          const int chunk = pass * 2 + c16;
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
               make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
         }
       }
-      tmem_st_wait();
       fence_async_smem();
       fence_before_sync();
-      mbar_arrive(&bars.p_ready);
+      mbar_arrive(&bars.p2_ready);               // dK_t and dQ_t may read dS^T
       ++t;
     }
     if (!ok && lane == 0) fail();

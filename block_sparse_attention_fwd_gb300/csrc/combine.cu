@@ -5,10 +5,15 @@
 // parts with LSE_p = -inf carry no weight; a row with no finite part gets
 // O = 0 and LSE = -inf.
 //
-// One warp per (b, r, h) row: lane p < parts holds LSE_p, the warp reduces the
-// max and the weight sum with shuffles, then every lane accumulates d/32
-// elements of every part in fp32 (coalesced 128/256-byte row reads).  The
-// pass is bound by HBM: parts*(2d+4) bytes in, 2d+4 bytes out per row.
+// The pass is bound by HBM: parts*(2d+4) bytes in, 2d+4 bytes out per row.
+// Thread = EPT consecutive elements (EPT/8 16-byte loads per part) of one
+// row; rows are numbered in the LSE's [B, H, n] order, so the threads of a
+// warp read LSE values of consecutive rows and whole 2d-byte output rows.
+// Every thread of a row forms the same weights from the parts' LSEs (a
+// broadcast read).  The parts are taken GP at a time and all loads of a group
+// are issued before any is used: (EPT, GP) = (16, 2) for up to two parts,
+// (8, 4) otherwise, which keeps 64 B per thread in flight at a register count
+// that leaves the SM well occupied.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,61 +21,90 @@ namespace bl {
 
 namespace {
 
-template <int D>
+__device__ __forceinline__ void fma_bf16x8(float* acc, const uint4& raw, float w) {
+  const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[e]));
+    acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
+    acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
+  }
+}
+
+template <int D, int EPT, int GP>
 __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ o_parts,
                                                       const float* __restrict__ lse_parts,
                                                       __nv_bfloat16* __restrict__ o,
                                                       float* __restrict__ lse, int parts, int B,
                                                       int n, int H) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  constexpr int TPR = D / EPT;   // threads per row
+  constexpr int NV = EPT / 8;    // 16-byte vectors per part
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t rows = (int64_t)B * n * H;
-  if (row >= rows) return;
-  const int h = (int)(row % H);
-  const int64_t br = row / H;
-  const int r = (int)(br % n);
-  const int b = (int)(br / n);
-  const int64_t lse_off = ((int64_t)b * H + h) * n + r;
-  const int64_t lse_stride = (int64_t)B * H * n;
-  const float lp = lane < parts ? lse_parts[lane * lse_stride + lse_off] : -INFINITY;
-  float m = lp;
+  const int64_t lrow = gid / TPR;          // row in [B, H, n] order
+  const int chunk = (int)(gid % TPR);
+  if (lrow >= rows) return;
+  const int r = (int)(lrow % n);
+  const int64_t bh = lrow / n;
+  const int h = (int)(bh % H);
+  const int b = (int)(bh / H);
+  const int64_t orow = ((int64_t)b * n + r) * H + h;   // row of the BSHD tensors
+  float m = -INFINITY;
+  for (int p = 0; p < parts; ++p) m = fmaxf(m, lse_parts[p * rows + lrow]);
+  float acc[EPT];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  constexpr int E = D / 32;   // elements per lane
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  if (isinf(m)) {   // no part saw a key for this row
-    if (lane == 0) lse[lse_off] = -INFINITY;
-  } else {
-    const float w_l = isinf(lp) ? 0.f : __expf(lp - m);
-    float tot = w_l;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    const float inv = 1.f / tot;
+  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+  float out_lse = -INFINITY;
+  if (!isinf(m)) {
+    float tot = 0.f;
     for (int p = 0; p < parts; ++p) {
-      const float w = __shfl_sync(0xffffffffu, w_l, p) * inv;
-      const __nv_bfloat16* src = o_parts + ((int64_t)p * rows + row) * D + lane * E;
-      if constexpr (E == 4) {
-        uint2 raw = *reinterpret_cast<const uint2*>(src);
-        float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.x));
-        float2 c = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.y));
-        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * c.x; acc[3] += w * c.y;
-      } else {
-        float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src));
-        acc[0] += w * a.x; acc[1] += w * a.y;
-      }
+      const float lp = lse_parts[p * rows + lrow];
+      tot += isinf(lp) ? 0.f : __expf(lp - m);
     }
-    if (lane == 0) lse[lse_off] = m + __logf(tot);
+    const float inv = 1.f / tot;
+    const __nv_bfloat16* src = o_parts + orow * D + chunk * EPT;
+    const int64_t pstride = rows * D;
+    for (int p = 0; p < parts; p += GP) {
+      uint4 raw[GP][NV];
+      float w[GP];
+#pragma unroll
+      for (int u = 0; u < GP; ++u) {
+        const bool in = p + u < parts;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + (int64_t)(p + u) * pstride);
+#pragma unroll
+        for (int vv = 0; vv < NV; ++vv) raw[u][vv] = in ? s4[vv] : make_uint4(0u, 0u, 0u, 0u);
+        const float lp = in ? lse_parts[(p + u) * rows + lrow] : -INFINITY;
+        w[u] = isinf(lp) ? 0.f : __expf(lp - m) * inv;
+      }
+#pragma unroll
+      for (int u = 0; u < GP; ++u)
+#pragma unroll
+        for (int vv = 0; vv < NV; ++vv) fma_bf16x8(acc + 8 * vv, raw[u][vv], w[u]);
+    }
+    out_lse = m + __logf(tot);
   }
-  __nv_bfloat16* dst = o + row * D + lane * E;
-  if constexpr (E == 4) {
-    uint2 w2;
-    w2.x = pack_bf16(acc[0], acc[1]);
-    w2.y = pack_bf16(acc[2], acc[3]);
-    *reinterpret_cast<uint2*>(dst) = w2;
+  if (chunk == 0) lse[lrow] = out_lse;
+  uint4* dst = reinterpret_cast<uint4*>(o + orow * D + chunk * EPT);
+#pragma unroll
+  for (int vv = 0; vv < NV; ++vv) {
+    const float* a = acc + 8 * vv;
+    dst[vv] = make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]),
+                         pack_bf16(a[6], a[7]));
+  }
+}
+
+template <int D>
+void launch_d(int parts, int B, int n, int H, const void* o_parts, const float* lse_parts,
+              void* o, float* lse, cudaStream_t st) {
+  const int64_t rows = (int64_t)B * n * H;
+  const auto* op = (const __nv_bfloat16*)o_parts;
+  auto* out = (__nv_bfloat16*)o;
+  if (parts <= 2) {
+    const unsigned blocks = (unsigned)((rows * (D / 16) + 255) / 256);
+    combine_kernel<D, 16, 2><<<blocks, 256, 0, st>>>(op, lse_parts, out, lse, parts, B, n, H);
   } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+    const unsigned blocks = (unsigned)((rows * (D / 8) + 255) / 256);
+    combine_kernel<D, 8, 4><<<blocks, 256, 0, st>>>(op, lse_parts, out, lse, parts, B, n, H);
   }
 }
 
@@ -78,14 +112,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
 
 cudaError_t launch_combine(int parts, int B, int n, int H, int d, const void* o_parts,
                            const float* lse_parts, void* o, float* lse, cudaStream_t st) {
-  const int64_t rows = (int64_t)B * n * H;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
   if (d == 128)
-    combine_kernel<128><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)o_parts, lse_parts,
-                                                (__nv_bfloat16*)o, lse, parts, B, n, H);
+    launch_d<128>(parts, B, n, H, o_parts, lse_parts, o, lse, st);
   else
-    combine_kernel<64><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)o_parts, lse_parts,
-                                               (__nv_bfloat16*)o, lse, parts, B, n, H);
+    launch_d<64>(parts, B, n, H, o_parts, lse_parts, o, lse, st);
   return cudaGetLastError();
 }
 

@@ -54,14 +54,29 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes or the hint (ns) runs out, instead of re-polling
+// the barrier.  Polling warps would otherwise spend shared-memory bandwidth
+// that the tensor core's shared-memory operands need.
+constexpr uint32_t kSuspendHintNs = 20000;
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete; false after the limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = saddr(bar);
   if (mbar_try(a, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(a, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  for (;;) {
+    if (mbar_try_sleep(a, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
 
