@@ -30,7 +30,8 @@ constexpr int QC = 64;  // query rows per chunk
 
 // D[b,h,r] = sum_d G_O[b,r,h,d] * O[b,r,h,d]: one warp per (b, r, h) row.
 // The same warp zeroes that row of the fp32 dQ accumulator, and block 0 the
-// status word, so no separate memset pass is needed.
+// status word and the word after it (the tcgen05 backward's work-item
+// counter), so no separate memset pass is needed.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ g_o,
@@ -40,7 +41,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t total = (int64_t)sh.B * sh.n * sh.H;
-  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    status[0] = 0;
+    status[1] = 0;
+  }
   if (row >= total) return;
   {
     float* z = dq_acc + row * D + lane * (D / 32);

@@ -94,8 +94,10 @@ typedef struct {
 size_t bl_tile_stats_elems(const bl_shape* shape);
 
 /* Bytes of device workspace bl_attn_bwd needs (16-byte aligned base):
- * D = rowsum(G_O * O) [B,H,n] fp32, the fp32 dQ accumulator [B,n,H,d] and a
- * device status word. */
+ * D = rowsum(G_O * O) [B,H,n] fp32, the fp32 dQ accumulator [B,n,H,d], a
+ * device status word and the backward kernel's work-item counter.  The call
+ * initialises all of it, so the workspace needs no clearing between calls;
+ * two calls in flight at the same time must not share one. */
 size_t bl_bwd_workspace_bytes(const bl_shape* shape);
 
 /* Exact attention forward ("Introducing BackLite", Backpropagation for
