@@ -21,7 +21,7 @@ BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "B
 # Every symbol include/bl_attn.h declares (checked by the CPU test suite).
 EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
            "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
-           "bl_attn_bwd_noalloc", "bl_lse_combine")
+           "bl_attn_bwd_noalloc", "bl_lse_combine", "bl_grad_error")
 
 
 class Shape(ctypes.Structure):
@@ -70,6 +70,8 @@ def load():
     lib.bl_attn_bwd_noalloc.restype = ctypes.c_int
     lib.bl_lse_combine.argtypes = [ctypes.c_int] * 5 + [P, P, P, P, P]
     lib.bl_lse_combine.restype = ctypes.c_int
+    lib.bl_grad_error.argtypes = [P, P, Z, P, P]
+    lib.bl_grad_error.restype = ctypes.c_int
     lib.bl_bwd_check_status.argtypes = [S, P, P]
     lib.bl_bwd_check_status.restype = ctypes.c_int
     lib.bl_status_string.argtypes = [ctypes.c_int]
@@ -227,3 +229,21 @@ def lse_combine(o_parts, lse_parts, o, lse):
     code = load().bl_lse_combine(P, B, n, H, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o),
                                  _ptr(lse), _stream(o.device))
     _check("bl_lse_combine", code)
+
+
+def grad_error(a, b, out=None):
+    """bl_grad_error: fp64 sums of (a-b)^2, b^2, a*b, a^2 over two bf16 tensors of
+    equal size (b the reference); returns (rel_l2, cos) as Python floats."""
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16 or a.numel() != b.numel():
+        raise ValueError("a and b must be bf16 tensors of the same size")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous")
+    if out is None:
+        out = torch.empty(4, dtype=torch.float64, device=a.device)
+    code = load().bl_grad_error(_ptr(a), _ptr(b), a.numel(), _ptr(out), _stream(a.device))
+    _check("bl_grad_error", code)
+    d2, b2, ab, a2 = out.tolist()
+    rel = (d2 / b2) ** 0.5 if b2 > 0 else (0.0 if d2 == 0 else float("inf"))
+    den = (b2 * a2) ** 0.5
+    cos = ab / den if den > 0 else (1.0 if d2 == 0 else 0.0)
+    return rel, cos

@@ -141,6 +141,13 @@ bl_status bl_lse_combine(int parts, int B, int n, int H, int d, const void* o_pa
                                         (cudaStream_t)stream));
 }
 
+bl_status bl_grad_error(const void* a, const void* b, size_t n, double* out, void* stream) {
+  if (!a || !b || !out || n == 0) return BL_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || (reinterpret_cast<uintptr_t>(out) & 7u))
+    return BL_ERR_INVALID_ARG;
+  return cuda_status(bl::launch_grad_error(a, b, (int64_t)n, out, (cudaStream_t)stream));
+}
+
 const char* bl_status_string(bl_status status) {
   switch (status) {
     case BL_OK: return "ok";

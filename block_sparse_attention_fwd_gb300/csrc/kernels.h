@@ -42,6 +42,9 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
                           cudaStream_t st);
 
 // LSE-combine of `parts` partial results (layouts in include/bl_attn.h).
+// Error sums of bf16 a against bf16 b (n elements) into out[4] (fp64).
+cudaError_t launch_grad_error(const void* a, const void* b, int64_t n, double* out,
+                              cudaStream_t st);
 cudaError_t launch_combine(int parts, int B, int n, int H, int d, const void* o_parts,
                            const float* lse_parts, void* o, float* lse, cudaStream_t st);
 

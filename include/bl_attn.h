@@ -170,6 +170,18 @@ bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace,
 bl_status bl_lse_combine(int parts, int B, int n, int H, int d, const void* o_parts,
                          const float* lse_parts, void* o, float* lse, void* stream);
 
+/* Error statistics of a gradient against a reference, for choosing negl_prob
+ * ("Introducing BackLite", Using Sparsity: the sparse backward is judged by
+ * the cosine similarity and relative L2 error of its gradients against the
+ * dense backward, and the post proposes tuning negl_prob to a target on
+ * them).  a and b: n bf16 values each (device, 16-byte aligned), b the
+ * reference.  out: 4 doubles of device memory (8-byte aligned), overwritten
+ * with
+ *   out[0] = sum (a - b)^2,  out[1] = sum b^2,  out[2] = sum a*b,  out[3] = sum a^2
+ * so rel-L2 = sqrt(out[0] / out[1]) and cos = out[2] / sqrt(out[1] * out[3]).
+ * Asynchronous on the stream.  Errors: BL_ERR_INVALID_ARG, BL_ERR_CUDA. */
+bl_status bl_grad_error(const void* a, const void* b, size_t n, double* out, void* stream);
+
 /* Size of the fixed device scratch array behind bl_attn_bwd_noalloc: 32 MiB
  * on every GPU that loads the library, held until the process exits. */
 #define BL_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

@@ -130,3 +130,12 @@ def test_causal_shape_checks(lib, kw, code):
     s = _shape(**kw)
     fake = ctypes.c_void_p(0x10000)
     assert lib.bl_attn_fwd(ctypes.byref(s), fake, fake, fake, 0.125, fake, fake, None, None) == code
+
+
+def test_grad_error_rejects_bad_arguments(lib):
+    ok = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    assert lib.bl_grad_error(None, ok, 8, ok, None) == 1
+    assert lib.bl_grad_error(ok, ok, 0, ok, None) == 1
+    assert lib.bl_grad_error(odd, ok, 8, ok, None) == 1
+    assert lib.bl_grad_error(ok, ok, 8, ctypes.c_void_p(0x10004), None) == 1
