@@ -358,15 +358,17 @@ def run_ours(args):
         "roofline_bwd": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16"],
                          "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16"],
                          "traffic": traffic.get("bwd_tc_kernel"),
-                         "kernel": "bl_attn_bwd call (bwd_tc_kernel + D pass + dQ convert + "
-                                   "memset), 10*d*valid rows*valid keys per kept tile",
+                         "kernel": "bl_attn_bwd call (D pass, which also zeroes the dQ "
+                                   "accumulator, + bwd_tc_kernel + dQ convert), 10*d*valid rows*"
+                                   "valid keys per kept tile",
                          "peak_src": pk["src"] + " burst"},
         "roofline_mask": {"bound": "hbm",
                           "achieved": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
                           "peak": pk["hbm"], "unit": "GB/s",
                           "frac": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9 / pk["hbm"],
-                          "traffic": traffic.get("mask_rows_kernel"),
-                          "kernel": "bl_mask_from_stats call (both kernels)"},
+                          "traffic": _sum_or_none(traffic, ("mask_rows_kernel", "q_lists_kernel")),
+                          "kernel": "bl_mask_from_stats call (mask_rows_kernel + q_lists_kernel)"},
+        # per step: forward 1, mask 2, backward 3 (D pass, tcgen05 pass, dQ convert)
         "gpu_launches": 6 * args.steps,
     }
     clk_s = clk.summary()
@@ -393,6 +395,13 @@ def _mask_bytes(w):
     lse = w.B * w.H * w.n * 4
     lists = w.B * w.H * w.T_r * w.T_c * (1 + 4 + 4) + w.B * w.H * (w.T_r + w.T_c) * 4
     return stats + lse + lists
+
+
+def _sum_or_none(traffic, kernels):
+    """Summed per-launch traffic of the kernels of one call, or None unless all
+    of them have a current measurement."""
+    vals = [traffic.get(k) for k in kernels]
+    return None if any(v is None for v in vals) else sum(vals)
 
 
 def _traffic(workload):

@@ -21,11 +21,17 @@
 //   which a parallel scan adds them.
 //
 // Kernel 1: one CTA per (query tile, head, batch).  Warps stream the
-// statistics of the tile's rows (coalesced 256/512-byte rows per key tile),
-// reduce d_ij, then the CTA sorts (key, E) pairs with a bitonic network in
-// shared memory, scans E, and writes the mask row plus the compacted kv list.
+// statistics of the tile's rows (coalesced 256/512-byte rows per key tile,
+// four key tiles in flight per warp) and reduce d_ij; then the CTA sorts
+// (key, E) pairs with a bitonic network, scans E, and writes the mask row
+// plus the compacted kv list.  With several CTAs per SM, one CTA's loads
+// overlap another's sort.  The shared arrays are sized by a capacity CAP (the
+// smallest power of two >= T_c, at least 256); at CAP = 256 each thread holds
+// one element and the network's stages closer than a warp run on shuffles.
 // Kernel 2: one warp per (key tile, head, batch) compacts the mask column
 // into the ascending q list with ballots.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -67,77 +73,75 @@ __device__ __forceinline__ uint32_t order_key(float d) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int RPL>  // rows per lane: block_q / 32
+template <int RPL, int CAP>  // rows per lane: block_q / 32; capacity >= T_c
 __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
     const float* __restrict__ stats, const float* __restrict__ lse, Shape sh,
     unsigned long long T, uint8_t* __restrict__ mask, int32_t* __restrict__ kv_idx,
     int32_t* __restrict__ kv_cnt, int32_t* __restrict__ nan_count) {
-  __shared__ float s_d[kMaxTc];
-  __shared__ unsigned long long s_key[kMaxTc];
-  __shared__ unsigned long long s_E[kMaxTc];
+  __shared__ float s_d[CAP];
+  __shared__ unsigned long long s_key[CAP];
+  __shared__ unsigned long long s_E[CAP];
   __shared__ unsigned long long s_wsum[kMaskThreads / 32];
   __shared__ int s_wcnt[kMaskThreads / 32];
-  __shared__ uint8_t s_act[kMaxTc];
+  __shared__ uint8_t s_act[CAP];
 
   const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Tc = sh.T_c;
   const int64_t bh = (int64_t)b * sh.H + h;
-  const int r0 = i * sh.block_q + lane * RPL;
-
-  float lrow[RPL];
-  bool valid[RPL];
-#pragma unroll
-  for (int e = 0; e < RPL; ++e) {
-    valid[e] = (r0 + e) < sh.n;
-    lrow[e] = valid[e] ? lse[bh * sh.n + r0 + e] : 0.f;
-  }
-  const float* st = stats + bh * sh.T_c * sh.n_pad + r0;
-  // key tiles with no attending pair (causal / window) have statistic -inf:
-  // their d is -inf without a load, and they are never kept
   int k_lo, k_hi;
   key_tile_range(sh, i, k_lo, k_hi);
-  constexpr int NW = kMaskThreads / 32;
-  constexpr int UNR = 4;   // key tiles in flight per warp
-  for (int j0 = warp; j0 < Tc; j0 += NW * UNR) {
-    float vals[UNR][RPL];
+  {
+    const int r0 = i * sh.block_q + lane * RPL;
+    float lrow[RPL];
+    bool valid[RPL];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int j = j0 + u * NW;
-      if (j >= Tc) continue;
-      if (j < k_lo || j > k_hi) {
-#pragma unroll
-        for (int e = 0; e < RPL; ++e) vals[u][e] = -INFINITY;
-        continue;
-      }
-      if constexpr (RPL == 4) {
-        float4 x = *reinterpret_cast<const float4*>(st + (int64_t)j * sh.n_pad);
-        vals[u][0] = x.x; vals[u][1] = x.y; vals[u][2] = x.z; vals[u][3] = x.w;
-      } else {
-        float2 x = *reinterpret_cast<const float2*>(st + (int64_t)j * sh.n_pad);
-        vals[u][0] = x.x; vals[u][1] = x.y;
-      }
+    for (int e = 0; e < RPL; ++e) {
+      valid[e] = (r0 + e) < sh.n;
+      lrow[e] = valid[e] ? lse[bh * sh.n + r0 + e] : 0.f;
     }
+    const float* st = stats + bh * sh.T_c * sh.n_pad + r0;
+    constexpr int NW = kMaskThreads / 32;
+    constexpr int UNR = 4;   // key tiles in flight per warp
+    for (int j0 = warp; j0 < Tc; j0 += NW * UNR) {
+      float vals[UNR][RPL];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) {
-      const int j = j0 + u * NW;
-      if (j >= Tc) continue;   // warp-uniform
-      float mx = -INFINITY;
-      bool nan = false;
+      for (int u = 0; u < UNR; ++u) {
+        const int j = j0 + u * NW;
+        if (j >= Tc || j < k_lo || j > k_hi) {
 #pragma unroll
-      for (int e = 0; e < RPL; ++e) {
-        if (!valid[e]) continue;
-        float dv = __fsub_rn(vals[u][e], lrow[e]);
-        if (isnan(dv)) nan = true;
-        else mx = fmaxf(mx, dv);
+          for (int e = 0; e < RPL; ++e) vals[u][e] = -INFINITY;
+          continue;
+        }
+        if constexpr (RPL == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(st + (int64_t)j * sh.n_pad);
+          vals[u][0] = x.x; vals[u][1] = x.y; vals[u][2] = x.z; vals[u][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(st + (int64_t)j * sh.n_pad);
+          vals[u][0] = x.x; vals[u][1] = x.y;
+        }
       }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      bool any_nan = __any_sync(0xffffffffu, nan);
-      if (lane == 0) {
-        float dv = any_nan ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
-        if (dv == 0.f) dv = 0.f;  // -0 -> +0
-        s_d[j] = dv;
+      for (int u = 0; u < UNR; ++u) {
+        const int j = j0 + u * NW;
+        if (j >= Tc) continue;   // warp-uniform
+        float mx = -INFINITY;
+        bool nan = false;
+#pragma unroll
+        for (int e = 0; e < RPL; ++e) {
+          if (!valid[e]) continue;
+          const float dv = __fsub_rn(vals[u][e], lrow[e]);
+          if (isnan(dv)) nan = true;
+          else mx = fmaxf(mx, dv);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const bool any_nan = __any_sync(0xffffffffu, nan);
+        if (lane == 0) {
+          float dv = any_nan ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
+          if (dv == 0.f) dv = 0.f;  // -0 -> +0
+          s_d[j] = dv;
+        }
       }
     }
   }
@@ -145,9 +149,10 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
 
   int P2 = 1;
   while (P2 < Tc) P2 <<= 1;
+  if (CAP == kMaskThreads) P2 = CAP;   // the register network sorts all CAP entries
   int local_nan = 0;
   for (int m = tid; m < P2; m += kMaskThreads) {
-    unsigned long long key = ~0ull, E = 0ull;
+    unsigned long long key = ~0ull;
     if (m < Tc) {
       float dv = s_d[m];
       if (isnan(dv)) {
@@ -155,12 +160,10 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
         ++local_nan;
       } else {
         key = ((unsigned long long)order_key(dv) << 32) | (unsigned)m;
-        E = detexp_fixed40(dv);
       }
       s_act[m] = 1;
     }
     s_key[m] = key;
-    s_E[m] = E;
   }
   if (nan_count) {
     local_nan = __reduce_add_sync(0xffffffffu, local_nan);
@@ -168,29 +171,57 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
   }
   __syncthreads();
 
-  // bitonic sort of (key, E) ascending by key
-  for (int kk = 2; kk <= P2; kk <<= 1) {
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      for (int tt = tid; tt < (P2 >> 1); tt += kMaskThreads) {
-        int a = (tt / jj) * 2 * jj + (tt % jj);
-        int c = a + jj;
-        bool up = (a & kk) == 0;
-        unsigned long long ka = s_key[a], kc = s_key[c];
-        if ((ka > kc) == up) {
-          s_key[a] = kc;
-          s_key[c] = ka;
-          unsigned long long ea = s_E[a];
-          s_E[a] = s_E[c];
-          s_E[c] = ea;
+  // bitonic sort of the keys ascending (unique but for the padding, which is
+  // equal and last); E follows from d once the order is known
+  if constexpr (CAP == kMaskThreads) {
+    // one element per thread: partners closer than a warp swap through
+    // shuffles, the six stages with stride >= 32 through shared memory
+    unsigned long long key = s_key[tid];
+    for (int kk = 2; kk <= CAP; kk <<= 1) {
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        unsigned long long pk;
+        if (jj >= 32) {
+          __syncthreads();
+          s_key[tid] = key;
+          __syncthreads();
+          pk = s_key[tid ^ jj];
+        } else {
+          pk = __shfl_xor_sync(0xffffffffu, key, jj);
         }
+        // the lower element of an ascending pair keeps the smaller key
+        const bool up = (tid & kk) == 0, lower = (tid & jj) == 0;
+        if ((lower == up) ? (pk < key) : (pk > key)) key = pk;
       }
-      __syncthreads();
+    }
+    __syncthreads();
+    s_key[tid] = key;
+  } else {
+    for (int kk = 2; kk <= P2; kk <<= 1) {
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        for (int tt = tid; tt < (P2 >> 1); tt += kMaskThreads) {
+          const int a = 2 * tt - (tt & (jj - 1));   // pair (a, a + jj), jj a power of two
+          const int c = a + jj;
+          const bool up = (a & kk) == 0;
+          const unsigned long long ka = s_key[a], kc = s_key[c];
+          if ((ka > kc) == up) {
+            s_key[a] = kc;
+            s_key[c] = ka;
+          }
+        }
+        __syncthreads();
+      }
     }
   }
+  // E in sorted order (0 for NaN and padding keys, which sort last)
+  for (int m = tid; m < P2; m += kMaskThreads) {
+    const unsigned long long key = s_key[m];
+    s_E[m] = (key >> 32) != 0xffffffffull ? detexp_fixed40(s_d[(int)(key & 0xffffffffull)]) : 0ull;
+  }
+  __syncthreads();
 
   // inclusive scan of E in sorted order; count positions with prefix < T
   // among the non-NaN entries (NaN and padding keys sort last).
-  constexpr int PER = kMaxTc / kMaskThreads;  // <= 8 elements per thread
+  constexpr int PER = CAP / kMaskThreads;  // <= 8 elements per thread
   int per = (P2 + kMaskThreads - 1) / kMaskThreads;
   int base = tid * per;
   unsigned long long run = 0ull;
@@ -280,12 +311,20 @@ cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
                         cudaStream_t st) {
   if (sh.T_c > kMaxTc) return cudaErrorInvalidValue;
   dim3 g1(sh.T_r, sh.H, sh.B);
+  auto rows = [&](auto rpl, auto cap) {
+    mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value>
+        <<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx, kv_cnt, nan_count);
+  };
+  auto by_cap = [&](auto rpl) {
+    if (sh.T_c <= 256) rows(rpl, std::integral_constant<int, 256>{});
+    else if (sh.T_c <= 512) rows(rpl, std::integral_constant<int, 512>{});
+    else if (sh.T_c <= 1024) rows(rpl, std::integral_constant<int, 1024>{});
+    else rows(rpl, std::integral_constant<int, 2048>{});
+  };
   if (sh.block_q == 128)
-    mask_rows_kernel<4><<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx,
-                                                     kv_cnt, nan_count);
+    by_cap(std::integral_constant<int, 4>{});
   else
-    mask_rows_kernel<2><<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx,
-                                                     kv_cnt, nan_count);
+    by_cap(std::integral_constant<int, 2>{});
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2((sh.T_c + 7) / 8, sh.H, sh.B);
