@@ -22,7 +22,9 @@
 //   R_S  [0,128)        S^T; after the softmax, P^T (bf16 pairs) in its
 //                       columns [0,32) and [64,96), read as the TMEM A operand
 //                       of dV += P^T dO
-//   R_dP [128,256)      dP^T; after the softmax, the dQ tile dS K
+//   R_dP [128,256)      dP^T; after the softmax, dS^T (bf16 pairs) in its
+//                       columns [0,32) and [64,96), the TMEM A operand of
+//                       dK += dS^T Q; then the dQ tile dS K (issued after dK)
 //   dV   [256,256+d)    dK [256+d,256+2d)
 // Per tile the issuer queues dV as soon as the softmax has written P^T
 // (first phase) and the next tile's S^T right behind it, so S^T runs while
@@ -47,8 +49,9 @@
 //               item ahead of the other roles.
 //   warps 4-7   softmax, query columns 0-63; warps 8-11 columns 64-127.
 //               Thread = key row: S^T, dP^T rows from TMEM -> P^T (TMEM) and
-//               dS^T (bf16, swizzled shared memory); after an item's last
-//               tile they write dV (warps 4-7) and s dK (warps 8-11).
+//               dS^T (TMEM for dK, and bf16 swizzled shared memory, where dQ
+//               reads it transposed); after an item's last tile they write
+//               dV (warps 4-7) and s dK (warps 8-11).
 //   warps 12-15 dQ drain: thread = query row; the dQ tile goes from TMEM
 //               through a 128-byte-swizzled staging buffer into the fp32
 //               accumulator with TMA bulk reduce-adds (whole-line L2 adds).
@@ -423,12 +426,13 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
           if (!ok) break;
           fence_after_sync();
           const uint32_t dsb = opaque(sDS);
-          const uint64_t dsk = sdesc_sw128(dsb, 16, 1024);        // dS^T, K-major
           const uint64_t qmn = sdesc_sw128(slot_addr(2 * t), C::CHUNK, 1024);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)        // dK += dS^T Q
-            mma_ss(tmem + C::T_DK, dsk + (((ks >> 2) * C::CHUNK + (ks & 3) * 32) >> 4),
-                   qmn + ks * (2048 >> 4), C::ID_G, (!first || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks) {      // dK += dS^T Q  (dS^T from TMEM)
+            const uint32_t dcol = C::T_DP + (ks >> 2) * 64 + (ks & 3) * 8;
+            mma_ts(tmem + C::T_DK, tmem + dcol, qmn + ks * (2048 >> 4), C::ID_G,
+                   (!first || ks > 0) ? 1u : 0u);
+          }
           mma_commit(&bars.empty[t & 1]);       // Q_t's slot
           if (!next) mma_commit(&bars.acc_full);  // dV, dK of this item are final
           // dQ = dS K into R_dP (dP^T was consumed by the softmax)
@@ -627,7 +631,11 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
                 make_uint4(dk[4 * c16], dk[4 * c16 + 1], dk[4 * c16 + 2], dk[4 * c16 + 3]);
           }
+          // and as bf16 pairs over dP^T columns already read, the TMEM A
+          // operand of dK += dS^T Q
+          tmem_st8(lane_base + C::T_DP + half * 64 + pass * 8, dk);
         }
+        tmem_st_wait();
         fence_async_smem();
         fence_before_sync();
         mbar_arrive(&bars.p2_ready);               // dK_t and dQ_t may read dS^T
