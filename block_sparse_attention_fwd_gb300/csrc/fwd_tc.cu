@@ -184,12 +184,18 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       }
       for (int jj = 0; ok && jj < nj; ++jj) {
         const bool more = jj + 1 < nj;
-        if (more)
-          ok = !failed(&s_fail) &&
-               mbar_wait(&bars.k_full[(jj + 1) % C::NK], ((jj + 1) / C::NK) & 1);
-        if (ok) ok = mbar_wait(&bars.v_full[jj % C::NV], (jj / C::NV) & 1);
+        // the three phases the next group needs, tested together so that
+        // their shared-memory round trips overlap; a blocking wait only for
+        // one that has not completed yet
+        const uint32_t kp = ((jj + 1) / C::NK) & 1, vp = (jj / C::NV) & 1;
+        const uint32_t rd =
+            mbar_test3(saddr(&bars.k_full[(jj + 1) % C::NK]), kp,
+                       saddr(&bars.v_full[jj % C::NV]), vp, saddr(&bars.p_ready[0]), jj & 1);
+        if (more && !(rd & 1))
+          ok = !failed(&s_fail) && mbar_wait(&bars.k_full[(jj + 1) % C::NK], kp);
+        if (ok && !(rd & 2)) ok = mbar_wait(&bars.v_full[jj % C::NV], vp);
         for (int t = 0; ok && t < ntile; ++t) {
-          ok = mbar_wait(&bars.p_ready[t], jj & 1);
+          ok = (t == 0 && (rd & 4)) || mbar_wait(&bars.p_ready[t], jj & 1);
           if (!ok) break;
           fence_after_sync();
           issue_pv(t, jj);

@@ -69,6 +69,26 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking tests of up to three barrier phases, issued back to back so
+// that their shared-memory round trips overlap (a lone mbarrier operation
+// can wait hundreds of cycles behind the tensor core's operand reads).  Bit i
+// of the result is set when phase i has completed.
+__device__ __forceinline__ uint32_t mbar_test3(uint32_t a0, uint32_t p0, uint32_t a1, uint32_t p1,
+                                               uint32_t a2, uint32_t p2) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred q0, q1, q2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n"
+      " selp.u32 %0, 1, 0, q0;\n"
+      " @q1 or.b32 %0, %0, 2;\n"
+      " @q2 or.b32 %0, %0, 4;\n}\n"
+      : "=r"(r)
+      : "r"(a0), "r"(p0), "r"(a1), "r"(p1), "r"(a2), "r"(p2)
+      : "memory");
+  return r;
+}
 // Wait for the phase with the given parity to complete; false after the limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = saddr(bar);
