@@ -70,9 +70,9 @@ __device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Non-blocking tests of up to three barrier phases, issued back to back so
-// that their shared-memory round trips overlap (a lone mbarrier operation
-// can wait hundreds of cycles behind the tensor core's operand reads).  Bit i
-// of the result is set when phase i has completed.
+// that their round trips overlap (on a thread that issues MMAs, one mbarrier
+// operation was measured at hundreds of cycles even on a completed phase).
+// Bit i of the result is set when phase i has completed.
 __device__ __forceinline__ uint32_t mbar_test3(uint32_t a0, uint32_t p0, uint32_t a1, uint32_t p1,
                                                uint32_t a2, uint32_t p2) {
   uint32_t r;
