@@ -58,7 +58,10 @@ struct FCfg {
 };
 
 struct FBars {
-  uint64_t q, k_full[3], k_empty[3], v_full[2], v_empty[2];
+  // done[u % 3] completes when every product up to S(u) has: K_u (read by
+  // S(u)) and V_(u-1) (read by PV(u-1)) are free.  One commit per key tile
+  // releases both rings.
+  uint64_t q, k_full[3], v_full[2], done[3];
   uint64_t s_full[2], p_ready[2], o_done[2];
 };
 
@@ -97,12 +100,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     mbar_init(&bars.q, 1);
     for (int s = 0; s < C::NK; ++s) {
       mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.done[s], 1);
     }
-    for (int s = 0; s < C::NV; ++s) {
-      mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.v_empty[s], 1);
-    }
+    for (int s = 0; s < C::NV; ++s) mbar_init(&bars.v_full[s], 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
       mbar_init(&bars.p_ready[t], 128);
@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
                       h, (2 * pair + t) * 128, b);
       auto load_v = [&](int jv) -> bool {   // jv counts visits
         const int sv = jv % C::NV;
-        if (!mbar_wait(&bars.v_empty[sv], ((jv / C::NV) & 1) ^ 1)) return false;
+        // V_(jv-2), the slot's previous tile, is free once done for u = jv - 1
+        if (jv >= C::NV && !mbar_wait(&bars.done[(jv - 1) % 3], ((jv - 1) / 3) & 1)) return false;
         mbar_expect_tx(&bars.v_full[sv], C::TILE_BYTES);
         for (int c = 0; c < C::CHK; ++c)
           tma_load_4d(sm + C::OFF_V + sv * C::TILE_BYTES + c * C::CHUNK, &tm_v, &bars.v_full[sv],
@@ -142,7 +143,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       for (int jj = 0; ok && jj <= nj; ++jj) {
         if (jj < nj) {
           const int sk = jj % C::NK;
-          ok = !failed(&s_fail) && mbar_wait(&bars.k_empty[sk], ((jj / C::NK) & 1) ^ 1);
+          // K_(jj-3), the slot's previous tile, is free once done for u = jj - 3
+          ok = !failed(&s_fail) &&
+               (jj < C::NK || mbar_wait(&bars.done[sk], ((jj - C::NK) / 3) & 1));
           if (!ok) break;
           mbar_expect_tx(&bars.k_full[sk], C::TILE_BYTES);
           for (int c = 0; c < C::CHK; ++c)
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       if (ok) {
         fence_after_sync();
         for (int t = 0; t < ntile; ++t) issue_s(t, 0);
-        mma_commit(&bars.k_empty[0]);
+        mma_commit(&bars.done[0]);
       }
       for (int jj = 0; ok && jj < nj; ++jj) {
         const bool more = jj + 1 < nj;
@@ -203,8 +206,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
           if (more) issue_s(t, jj + 1);
         }
         if (!ok) break;
-        mma_commit(&bars.v_empty[jj % C::NV]);
-        if (more) mma_commit(&bars.k_empty[(jj + 1) % C::NK]);
+        if (more) mma_commit(&bars.done[(jj + 1) % 3]);   // K_(jj+1) and V_jj are free
       }
       if (!ok) fail();
       for (int t = 0; t < 2; ++t) mma_commit(&bars.o_done[t]);
