@@ -68,6 +68,14 @@ __device__ __forceinline__ uint64_t detexp_fixed40(float d) {
   return (uint64_t)__float2ull_rn(ceilf(s));
 }
 
+// max that propagates NaN: one operation carries both the maximum and the
+// "some term is NaN" flag of the reduction
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t order_key(float d) {
   uint32_t u = __float_as_uint(d);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -125,20 +133,16 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
       for (int u = 0; u < UNR; ++u) {
         const int j = j0 + u * NW;
         if (j >= Tc) continue;   // warp-uniform
+        // max over the tile's rows of fl32(stat - lse), NaN if any term is
         float mx = -INFINITY;
-        bool nan = false;
 #pragma unroll
-        for (int e = 0; e < RPL; ++e) {
-          if (!valid[e]) continue;
-          const float dv = __fsub_rn(vals[u][e], lrow[e]);
-          if (isnan(dv)) nan = true;
-          else mx = fmaxf(mx, dv);
-        }
+        for (int e = 0; e < RPL; ++e)
+          if (valid[e]) mx = max_nan(mx, __fsub_rn(vals[u][e], lrow[e]));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const bool any_nan = __any_sync(0xffffffffu, nan);
+        for (int off = 16; off > 0; off >>= 1)
+          mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         if (lane == 0) {
-          float dv = any_nan ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
+          float dv = isnan(mx) ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
           if (dv == 0.f) dv = 0.f;  // -0 -> +0
           s_d[j] = dv;
         }
