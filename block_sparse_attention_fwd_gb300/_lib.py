@@ -21,7 +21,9 @@ BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "B
 # Every symbol include/bl_attn.h declares (checked by the CPU test suite).
 EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
            "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
-           "bl_attn_bwd_noalloc", "bl_lse_combine", "bl_grad_error")
+           "bl_attn_bwd_noalloc", "bl_lse_combine", "bl_grad_error", "bl_varlen_layout",
+           "bl_attn_fwd_varlen", "bl_mask_from_stats_varlen", "bl_attn_bwd_varlen",
+           "bl_varlen_bwd_check_status")
 
 
 class Shape(ctypes.Structure):
@@ -34,6 +36,21 @@ class Lists(ctypes.Structure):
     _fields_ = [("mask", ctypes.c_void_p), ("kv_idx", ctypes.c_void_p),
                 ("kv_cnt", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
                 ("q_cnt", ctypes.c_void_p), ("nan_count", ctypes.c_void_p)]
+
+
+class VarlenStruct(ctypes.Structure):
+    _fields_ = [("nseq", ctypes.c_int), ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
+                ("H", ctypes.c_int), ("Hk", ctypes.c_int), ("d", ctypes.c_int),
+                ("block_q", ctypes.c_int), ("block_k", ctypes.c_int), ("causal", ctypes.c_int),
+                ("window", ctypes.c_int)]
+
+
+class VarlenSizes(ctypes.Structure):
+    _fields_ = [("total", ctypes.c_size_t), ("lse", ctypes.c_size_t),
+                ("tile_stats", ctypes.c_size_t), ("mask", ctypes.c_size_t),
+                ("kv_cnt", ctypes.c_size_t), ("q_idx", ctypes.c_size_t),
+                ("q_cnt", ctypes.c_size_t), ("bwd_workspace_bytes", ctypes.c_size_t),
+                ("groups", ctypes.c_int)]
 
 
 class BLError(RuntimeError):
@@ -74,6 +91,18 @@ def load():
     lib.bl_grad_error.restype = ctypes.c_int
     lib.bl_bwd_check_status.argtypes = [S, P, P]
     lib.bl_bwd_check_status.restype = ctypes.c_int
+    V = ctypes.POINTER(VarlenStruct)
+    lib.bl_varlen_layout.argtypes = [V, ctypes.POINTER(VarlenSizes)]
+    lib.bl_varlen_layout.restype = ctypes.c_int
+    lib.bl_attn_fwd_varlen.argtypes = [V, P, P, P, F, P, P, P, P]
+    lib.bl_attn_fwd_varlen.restype = ctypes.c_int
+    lib.bl_mask_from_stats_varlen.argtypes = [V, P, P, D, ctypes.POINTER(Lists), P]
+    lib.bl_mask_from_stats_varlen.restype = ctypes.c_int
+    lib.bl_attn_bwd_varlen.argtypes = [V, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P,
+                                       P, Z, P]
+    lib.bl_attn_bwd_varlen.restype = ctypes.c_int
+    lib.bl_varlen_bwd_check_status.argtypes = [V, P, P]
+    lib.bl_varlen_bwd_check_status.restype = ctypes.c_int
     lib.bl_status_string.argtypes = [ctypes.c_int]
     lib.bl_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -247,3 +276,106 @@ def grad_error(a, b, out=None):
     den = (b2 * a2) ** 0.5
     cos = ab / den if den > 0 else (1.0 if d2 == 0 else 0.0)
     return rel, cos
+
+
+# --- packed variable-length batches ------------------------------------------
+
+class Varlen:
+    """A packed batch description for the bl_*_varlen calls.  Holds the host
+    copy of cu_seqlens (nseq + 1 int32 offsets) that the C struct points at,
+    and the element counts bl_varlen_layout reports."""
+
+    def __init__(self, cu_seqlens, H, Hk, d, block_q=128, block_k=128, causal=0, window=0):
+        cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist")
+                               else cu_seqlens)]
+        self.cu_seqlens = cu
+        self._cu = (ctypes.c_int32 * len(cu))(*cu)
+        self.struct = VarlenStruct(len(cu) - 1, self._cu, H, Hk, d, block_q, block_k,
+                                   int(causal), int(window))
+        self.H, self.Hk, self.d = H, Hk, d
+        self.block_q, self.block_k = block_q, block_k
+        self.causal, self.window = int(causal), int(window)
+        sz = VarlenSizes()
+        _check("bl_varlen_layout", load().bl_varlen_layout(ctypes.byref(self.struct),
+                                                           ctypes.byref(sz)))
+        self.sizes = {f: getattr(sz, f) for f, _ in VarlenSizes._fields_}
+
+    @property
+    def total(self):
+        return self.sizes["total"]
+
+    def seq_shape(self, s):
+        """The fixed-length shape (B = 1) of sequence s alone."""
+        n = self.cu_seqlens[s + 1] - self.cu_seqlens[s]
+        return make_shape(1, n, self.H, self.Hk, self.d, self.block_q, self.block_k,
+                          self.causal, self.window)
+
+
+def alloc_varlen_lists(vl: Varlen, device) -> dict:
+    z = vl.sizes
+    return {
+        "mask": torch.empty(z["mask"], dtype=torch.uint8, device=device),
+        "kv_idx": torch.empty(z["mask"], dtype=torch.int32, device=device),
+        "kv_cnt": torch.empty(z["kv_cnt"], dtype=torch.int32, device=device),
+        "q_idx": torch.empty(z["q_idx"], dtype=torch.int32, device=device),
+        "q_cnt": torch.empty(z["q_cnt"], dtype=torch.int32, device=device),
+        "nan_count": torch.zeros((1,), dtype=torch.int32, device=device),
+    }
+
+
+def attn_fwd_varlen(vl: Varlen, q, k, v, scale, o, lse, tile_stats=None):
+    T, H, Hk, d = vl.total, vl.H, vl.Hk, vl.d
+    _need(q, torch.bfloat16, (T, H, d), "q")
+    _need(k, torch.bfloat16, (T, Hk, d), "k")
+    _need(v, torch.bfloat16, (T, Hk, d), "v")
+    _need(o, torch.bfloat16, (T, H, d), "o")
+    _need(lse, torch.float32, (vl.sizes["lse"],), "lse")
+    if tile_stats is not None:
+        _need(tile_stats, torch.float32, (vl.sizes["tile_stats"],), "tile_stats")
+    code = load().bl_attn_fwd_varlen(ctypes.byref(vl.struct), _ptr(q), _ptr(k), _ptr(v),
+                                     float(scale), _ptr(o), _ptr(lse), _ptr(tile_stats),
+                                     _stream(q.device))
+    _check("bl_attn_fwd_varlen", code)
+
+
+def mask_from_stats_varlen(vl: Varlen, tile_stats, lse, negl_prob, lists):
+    z = vl.sizes
+    _need(tile_stats, torch.float32, (z["tile_stats"],), "tile_stats")
+    _need(lse, torch.float32, (z["lse"],), "lse")
+    _need(lists["mask"], torch.uint8, (z["mask"],), "mask")
+    _need(lists["kv_idx"], torch.int32, (z["mask"],), "kv_idx")
+    _need(lists["kv_cnt"], torch.int32, (z["kv_cnt"],), "kv_cnt")
+    _need(lists["q_idx"], torch.int32, (z["q_idx"],), "q_idx")
+    _need(lists["q_cnt"], torch.int32, (z["q_cnt"],), "q_cnt")
+    ls = _lists_struct(lists)
+    code = load().bl_mask_from_stats_varlen(ctypes.byref(vl.struct), _ptr(tile_stats),
+                                            _ptr(lse), float(negl_prob), ctypes.byref(ls),
+                                            _stream(lse.device))
+    _check("bl_mask_from_stats_varlen", code)
+
+
+def attn_bwd_varlen(vl: Varlen, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, workspace):
+    T, H, Hk, d = vl.total, vl.H, vl.Hk, vl.d
+    for t, nm, sh in ((q, "q", (T, H, d)), (k, "k", (T, Hk, d)), (v, "v", (T, Hk, d)),
+                      (o, "o", (T, H, d)), (g_o, "g_o", (T, H, d)), (g_q, "g_q", (T, H, d)),
+                      (g_k, "g_k", (T, Hk, d)), (g_v, "g_v", (T, Hk, d))):
+        _need(t, torch.bfloat16, sh, nm)
+    _need(lse, torch.float32, (vl.sizes["lse"],), "lse")
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA uint8 tensor")
+    ls = None
+    if lists is not None:
+        _need(lists["q_idx"], torch.int32, (vl.sizes["q_idx"],), "q_idx")
+        _need(lists["q_cnt"], torch.int32, (vl.sizes["q_cnt"],), "q_cnt")
+        ls = _lists_struct(lists)
+    code = load().bl_attn_bwd_varlen(ctypes.byref(vl.struct), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(o), _ptr(g_o), _ptr(lse), float(scale),
+                                     ctypes.byref(ls) if ls is not None else None,
+                                     _ptr(g_q), _ptr(g_k), _ptr(g_v), _ptr(workspace),
+                                     workspace.numel(), _stream(q.device))
+    _check("bl_attn_bwd_varlen", code)
+
+
+def varlen_bwd_check_status(vl: Varlen, workspace) -> int:
+    return int(load().bl_varlen_bwd_check_status(ctypes.byref(vl.struct), _ptr(workspace),
+                                                 _stream(workspace.device)))

@@ -12,7 +12,9 @@ backward (Key properties).  ``BL_VERBOSE=1`` prints mask density per head
 after each mask pass (README, Debugging, names the same kind of switch).
 ``causal=True`` (optionally with ``window=W``) gives decoder attention, with
 the sliding windows of the "Introducing BackLite" post's Nanochat runs
-(Training Nanochat).
+(Training Nanochat).  ``BLAttention.varlen(q, k, v, cu_seqlens)`` runs the
+same chain on a packed variable-length batch ([total, heads, head_dim]
+tensors, host offsets cu_seqlens), each sequence attending only to itself.
 
 PyTorch only allocates memory and supplies the stream; all arithmetic runs in
 libbl_attn.so.
@@ -75,6 +77,36 @@ class _BLAttnFn(torch.autograd.Function):
         return g_q, g_k, g_v, None, None, None, None, None, None, None
 
 
+class _BLAttnVarlenFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, vl, scale, negl_prob):
+        o = torch.empty_like(q)
+        lse = torch.empty(vl.sizes["lse"], dtype=torch.float32, device=q.device)
+        stats = None
+        if negl_prob > 0:
+            stats = torch.empty(vl.sizes["tile_stats"], dtype=torch.float32, device=q.device)
+        _lib.attn_fwd_varlen(vl, q, k, v, scale, o, lse, stats)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.stats = stats
+        ctx.cfg = (vl, scale, negl_prob)
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, g_o, _g_lse):
+        q, k, v, o, lse = ctx.saved_tensors
+        vl, scale, negl_prob = ctx.cfg
+        lists = None
+        if ctx.stats is not None:
+            lists = _lib.alloc_varlen_lists(vl, q.device)
+            _lib.mask_from_stats_varlen(vl, ctx.stats, lse, negl_prob, lists)
+        g_q, g_k, g_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(vl.sizes["bwd_workspace_bytes"], dtype=torch.uint8, device=q.device)
+        _lib.attn_bwd_varlen(vl, q, k, v, o, g_o.contiguous(), lse, scale, lists, g_q, g_k, g_v,
+                             ws)
+        return g_q, g_k, g_v, None, None, None
+
+
 class BLAttention(torch.nn.Module):
     """Attention whose backward skips the lightest tiles (negl_prob of the mass)."""
 
@@ -99,4 +131,21 @@ class BLAttention(torch.nn.Module):
         q, k, v = (t.contiguous() for t in (query, key, value))
         o, lse = _BLAttnFn.apply(q, k, v, float(scale), self.negl_prob, bq, bk, tile_stats,
                                  int(self.causal), self.window)
+        return (o, lse) if return_softmax_lse else o
+
+    def varlen(self, query, key, value, cu_seqlens, scale=None, return_softmax_lse=False):
+        """The same attention on a packed batch: query [total, H, d], key/value
+        [total, Hk, d], cu_seqlens the nseq + 1 token offsets (a host sequence
+        or CPU tensor).  Returns O [total, H, d] and, if asked, the flat LSE
+        (per sequence a [H, n_s] block at offset H * cu_seqlens[s])."""
+        total, H, d = query.shape
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        bq, bk = default_tiles(total, d)
+        vl = _lib.Varlen(cu_seqlens, H, key.shape[1], d, self.block_q or bq, self.block_k or bk,
+                         int(self.causal), self.window)
+        if vl.total != total:
+            raise ValueError(f"cu_seqlens covers {vl.total} tokens, query has {total}")
+        q, k, v = (t.contiguous() for t in (query, key, value))
+        o, lse = _BLAttnVarlenFn.apply(q, k, v, vl, float(scale), self.negl_prob)
         return (o, lse) if return_softmax_lse else o

@@ -4,14 +4,13 @@
 #include <stdint.h>
 
 #include "../../include/bl_attn.h"
+#include "abi.h"
 #include "common.cuh"
 #include "kernels.h"
 
-namespace {
+namespace bl {
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bl_status check_shape(const bl_shape* s, bl::Shape* out) {
+bl_status check_shape(const bl_shape* s, Shape* out) {
   if (!s) return BL_ERR_INVALID_ARG;
   if (s->B < 1 || s->n < 1 || s->H < 1 || s->Hk < 1 || s->H % s->Hk != 0)
     return BL_ERR_INVALID_ARG;
@@ -23,7 +22,7 @@ bl_status check_shape(const bl_shape* s, bl::Shape* out) {
   if (s->window < 0 || (s->window > 0 && !s->causal)) return BL_ERR_INVALID_ARG;
   if ((s->causal || s->window) && (s->block_q != 128 || s->block_k != 128))
     return BL_ERR_UNSUPPORTED;
-  bl::Shape sh;
+  Shape sh;
   sh.B = s->B; sh.n = s->n; sh.H = s->H; sh.Hk = s->Hk; sh.d = s->d;
   sh.block_q = s->block_q; sh.block_k = s->block_k;
   sh.causal = s->causal; sh.window = s->window;
@@ -34,13 +33,14 @@ bl_status check_shape(const bl_shape* s, bl::Shape* out) {
   return BL_OK;
 }
 
-size_t ws_D_bytes(const bl::Shape& sh) {
-  size_t b = (size_t)sh.B * sh.H * sh.n * sizeof(float);
-  return (b + 255) & ~(size_t)255;
-}
-size_t ws_dq_bytes(const bl::Shape& sh) {
-  return (size_t)sh.B * sh.n * sh.H * sh.d * sizeof(float);
-}
+}  // namespace bl
+
+namespace {
+
+using bl::aligned16;
+using bl::check_shape;
+using bl::ws_D_bytes;
+using bl::ws_dq_bytes;
 
 bl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
 
@@ -57,7 +57,7 @@ size_t bl_tile_stats_elems(const bl_shape* shape) {
 size_t bl_bwd_workspace_bytes(const bl_shape* shape) {
   bl::Shape sh;
   if (check_shape(shape, &sh) != BL_OK) return 0;
-  return ws_D_bytes(sh) + ws_dq_bytes(sh) + 256;
+  return ws_D_bytes(sh) + ws_dq_bytes(sh) + bl::kWsStatusBytes;
 }
 
 bl_status bl_attn_fwd(const bl_shape* shape, const void* q, const void* k, const void* v,
@@ -84,11 +84,9 @@ bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats, con
   if (!aligned16(tile_stats) || !aligned16(lse)) return BL_ERR_INVALID_ARG;
   if (!(negl_prob >= 0.0) || !(negl_prob < 1.0)) return BL_ERR_INVALID_ARG;
   if (sh.T_c > 2048) return BL_ERR_UNSUPPORTED;
-  // T = ceil(negl_prob * 2^40): the product is exact in fp64.
-  unsigned long long T = (unsigned long long)ceil(negl_prob * 1099511627776.0);
-  return cuda_status(bl::launch_mask(sh, tile_stats, lse, T, lists->mask, lists->kv_idx,
-                                     lists->kv_cnt, lists->q_idx, lists->q_cnt,
-                                     lists->nan_count, (cudaStream_t)stream));
+  return cuda_status(bl::launch_mask(sh, tile_stats, lse, bl::mask_threshold(negl_prob),
+                                     lists->mask, lists->kv_idx, lists->kv_cnt, lists->q_idx,
+                                     lists->q_cnt, lists->nan_count, (cudaStream_t)stream));
 }
 
 bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k, const void* v,

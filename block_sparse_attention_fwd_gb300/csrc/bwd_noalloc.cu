@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "../../include/bl_attn.h"
+#include "abi.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -41,8 +42,6 @@ void* scratch_address() {
   return g_scratch_addr[dev];
 }
 
-size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 }  // namespace
 
 extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* k,
@@ -57,28 +56,21 @@ extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, c
   if (need > (size_t)BL_NOALLOC_SCRATCH_BYTES) return BL_ERR_WORKSPACE;
   const void* ptrs[] = {q, k, v, o, g_o, lse, g_q, g_k, g_v};
   for (const void* p : ptrs)
-    if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return BL_ERR_INVALID_ARG;
+    if (!p || !bl::aligned16(p)) return BL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
   if (lists && (!lists->q_idx || !lists->q_cnt)) return BL_ERR_INVALID_ARG;
   unsigned char* ws = static_cast<unsigned char*>(scratch_address());
   if (!ws) return BL_ERR_CUDA;
 
   bl::Shape sh;
-  sh.B = shape->B; sh.n = shape->n; sh.H = shape->H; sh.Hk = shape->Hk; sh.d = shape->d;
-  sh.block_q = shape->block_q; sh.block_k = shape->block_k;
-  sh.causal = shape->causal; sh.window = shape->window;
-  sh.T_r = (sh.n + sh.block_q - 1) / sh.block_q;
-  sh.T_c = (sh.n + sh.block_k - 1) / sh.block_k;
-  sh.n_pad = (int64_t)sh.T_r * sh.block_q;
+  if (bl::check_shape(shape, &sh) != BL_OK) return BL_ERR_INVALID_ARG;  // unreachable: need > 0
   // Same layout as the workspace of bl_attn_bwd.  The preprocessing kernel
   // that launch_bwd runs first writes every D entry and zeroes the dQ
   // accumulator and the status word, so nothing left by an earlier call leaks
   // into this one.
-  const size_t d_bytes = round256((size_t)sh.B * sh.H * sh.n * sizeof(float));
-  const size_t dq_bytes = (size_t)sh.B * sh.n * sh.H * sh.d * sizeof(float);
   float* ws_D = reinterpret_cast<float*>(ws);
-  float* ws_dq = reinterpret_cast<float*>(ws + d_bytes);
-  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + d_bytes + dq_bytes);
+  float* ws_dq = reinterpret_cast<float*>(ws + bl::ws_D_bytes(sh));
+  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + bl::ws_D_bytes(sh) + bl::ws_dq_bytes(sh));
   cudaError_t e = bl::launch_bwd(sh, q, k, v, o, g_o, lse, scale, lists ? lists->q_idx : nullptr,
                                  lists ? lists->q_cnt : nullptr, g_q, g_k, g_v, ws_D, ws_dq,
                                  ws_status, (cudaStream_t)stream);

@@ -200,3 +200,20 @@ def generate(w: Workload, seed: int = 0, with_grad_out: bool = True):
     else:
         out.append(None)
     return tuple(out)
+
+
+def generate_packed(w: Workload, lengths, seed: int = 0):
+    """A packed variable-length batch: sequence s of ``lengths`` is drawn as the
+    workload ``w`` with B = 1 and n = lengths[s] (seed ``seed + s``), and the
+    sequences are stacked along the token axis.  Returns (cu_seqlens, q, k, v,
+    g_o) with q, g_o [total, H, d] and k, v [total, Hk, d] CPU bf16 tensors;
+    empty sequences own no rows."""
+    cu = [0]
+    parts = []
+    for s, n in enumerate(lengths):
+        cu.append(cu[-1] + int(n))
+        if n:
+            ws = dataclasses.replace(w, B=1, n=int(n))
+            parts.append([x[0] for x in generate(ws, seed=seed + s)])
+    q, k, v, go = (torch.cat([p[i] for p in parts], dim=0).contiguous() for i in range(4))
+    return cu, q, k, v, go

@@ -209,6 +209,94 @@ bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* 
                               const float* lse, float scale, const bl_lists* lists,
                               void* g_q, void* g_k, void* g_v, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Packed variable-length batches.
+ *
+ * nseq sequences of lengths n_s = cu_seqlens[s+1] - cu_seqlens[s] are packed
+ * back to back along the token axis; a query attends only to keys of its own
+ * sequence.  The BackLite pages train on fixed-length batches and say
+ * nothing about packing; this is the plain reading of packing: the result
+ * for every sequence is exactly the result of the fixed-length call with
+ * B = 1, n = n_s on that sequence alone, and every per-sequence array is
+ * that call's array, stored one sequence after another.
+ *
+ * Tensors (total = cu_seqlens[nseq])
+ *   q, o, g_o, g_q : [total, H,  d] bf16, contiguous
+ *   k, v, g_k, g_v : [total, Hk, d] bf16, contiguous
+ *   lse            : per sequence a [H, n_s] fp32 block, at element offset
+ *                    H * cu_seqlens[s]
+ *   tile_stats     : per sequence a [H, T_c(s), T_r(s)*block_q] fp32 block,
+ *                    blocks back to back in sequence order
+ *   lists          : each field per sequence a block laid out as the
+ *                    fixed-length field with B = 1, blocks back to back;
+ *                    nan_count is one counter for the whole batch
+ * with T_r(s) = ceil(n_s / block_q), T_c(s) = ceil(n_s / block_k).
+ * bl_varlen_layout gives every size.  A sequence of length 0 owns nothing
+ * and launches nothing.
+ *
+ * Execution: the calls walk the sequences on the host and run the
+ * fixed-length kernels once per run of consecutive sequences of equal
+ * length (such a run is exactly a [count, n_s, ...] batch).  Nothing waits
+ * on the host between launches, so the calls can be captured in a CUDA
+ * graph.  lse only needs 4-byte alignment here; the other device pointers
+ * need 16 bytes, as in the fixed-length calls.
+ * ------------------------------------------------------------------------- */
+
+/* cu_seqlens: HOST array of nseq + 1 int32, cu_seqlens[0] = 0,
+ * non-decreasing, cu_seqlens[nseq] >= 1.  The other fields mean what they
+ * mean in bl_shape and obey the same limits. */
+typedef struct {
+  int nseq;
+  const int32_t* cu_seqlens;
+  int H, Hk, d;
+  int block_q, block_k;
+  int causal, window;
+} bl_varlen;
+
+/* Element counts (bytes for bwd_workspace_bytes) of a packed batch. */
+typedef struct {
+  size_t total;                /* packed tokens                                  */
+  size_t lse;                  /* fp32: H * total                                */
+  size_t tile_stats;           /* fp32: sum_s H * T_c(s) * T_r(s) * block_q      */
+  size_t mask;                 /* uint8 mask and int32 kv_idx: sum_s H*T_r*T_c   */
+  size_t kv_cnt;               /* int32: sum_s H * T_r(s)                        */
+  size_t q_idx;                /* int32: sum_s H * T_c(s) * T_r(s)               */
+  size_t q_cnt;                /* int32: sum_s H * T_c(s)                        */
+  size_t bwd_workspace_bytes;  /* workspace of bl_attn_bwd_varlen                */
+  int groups;                  /* launches of each kernel per call               */
+} bl_varlen_sizes;
+
+/* Validates *varlen and fills *sizes.  Errors: BL_ERR_INVALID_ARG (bad
+ * cu_seqlens or shape fields), BL_ERR_UNSUPPORTED (d or tile size). */
+bl_status bl_varlen_layout(const bl_varlen* varlen, bl_varlen_sizes* sizes);
+
+/* bl_attn_fwd over a packed batch (layouts above; tile_stats may be NULL). */
+bl_status bl_attn_fwd_varlen(const bl_varlen* varlen, const void* q, const void* k,
+                             const void* v, float scale, void* o, float* lse,
+                             float* tile_stats, void* stream);
+
+/* bl_mask_from_stats over a packed batch: the selection of every sequence
+ * uses only that sequence's statistics.  BL_ERR_UNSUPPORTED when a sequence
+ * has more than 2048 key tiles. */
+bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_stats,
+                                    const float* lse, double negl_prob,
+                                    const bl_lists* lists, void* stream);
+
+/* bl_attn_bwd over a packed batch.  workspace: at least
+ * sizes.bwd_workspace_bytes; runs of sequences reuse its D and dQ areas one
+ * after another on the stream and each has its own status word. */
+bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void* k,
+                             const void* v, const void* o, const void* g_o,
+                             const float* lse, float scale, const bl_lists* lists,
+                             void* g_q, void* g_k, void* g_v, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* bl_bwd_check_status for bl_attn_bwd_varlen: synchronises the stream and
+ * reports the worst status word of the call's runs (BL_ERR_TIMEOUT before
+ * BL_ERR_CORRUPT_LISTS before BL_OK). */
+bl_status bl_varlen_bwd_check_status(const bl_varlen* varlen, const void* workspace,
+                                     void* stream);
+
 /* Static description of a status code. */
 const char* bl_status_string(bl_status status);
 

@@ -6,5 +6,6 @@ code with the CUDA path.
 
 * ``attention``  -- exact forward, per-tile LSE statistics, masked backward.
 * ``mask_spec``  -- the canonical tile-selection rule (mask_from_stats).
+* ``varlen``     -- the three steps over packed variable-length batches.
 """
-from . import attention, mask_spec  # noqa: F401
+from . import attention, mask_spec, varlen  # noqa: F401

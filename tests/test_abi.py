@@ -139,3 +139,93 @@ def test_grad_error_rejects_bad_arguments(lib):
     assert lib.bl_grad_error(ok, ok, 0, ok, None) == 1
     assert lib.bl_grad_error(odd, ok, 8, ok, None) == 1
     assert lib.bl_grad_error(ok, ok, 8, ctypes.c_void_p(0x10004), None) == 1
+
+
+def _varlen(cu, **kw):
+    from block_sparse_attention_fwd_gb300 import _lib
+    a = dict(H=4, Hk=2, d=64, block_q=128, block_k=128, causal=0, window=0)
+    a.update(kw)
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    v = _lib.VarlenStruct(len(cu) - 1, arr, a["H"], a["Hk"], a["d"], a["block_q"],
+                          a["block_k"], a["causal"], a["window"])
+    return v, arr
+
+
+@pytest.mark.parametrize("cu,bq,bk", [
+    ([0, 1, 129, 257, 385, 1000, 1000, 1300], 128, 128),
+    ([0, 0, 300, 301, 301, 700], 64, 128),
+    ([0, 5000], 128, 64),
+    ([0, 64, 128, 192, 250, 250, 320], 64, 64)])
+def test_varlen_layout_matches_the_oracle_layout(lib, cu, bq, bk):
+    from block_sparse_attention_fwd_gb300 import _lib
+    from oracle import varlen as OV
+    v, arr = _varlen(cu, block_q=bq, block_k=bk)
+    sz = _lib.VarlenSizes()
+    assert lib.bl_varlen_layout(ctypes.byref(v), ctypes.byref(sz)) == 0
+    _, tot = OV.layout(cu, 4, bq, bk)
+    assert (sz.total, sz.lse, sz.tile_stats, sz.mask, sz.kv_cnt, sz.q_idx, sz.q_cnt) == \
+        (tot["total"], tot["lse"], tot["stats"], tot["mask"], tot["kv_cnt"], tot["q_idx"],
+         tot["q_cnt"])
+    # one launch group per run of equal non-zero lengths
+    lens = [b - a for a, b in zip(cu[:-1], cu[1:]) if b > a]
+    assert sz.groups == sum(1 for i, n in enumerate(lens) if i == 0 or lens[i - 1] != n)
+    assert sz.bwd_workspace_bytes >= max(4 * 4 * 64 * n for n in lens)
+
+
+@pytest.mark.parametrize("cu,kw,code", [
+    ([1, 5], {}, 1),                    # cu[0] != 0
+    ([0, 9, 4], {}, 1),                 # decreasing
+    ([0, 0, 0], {}, 1),                 # no tokens
+    ([0], {}, 1),                       # no sequence
+    ([0, 100], dict(d=96), 2),
+    ([0, 100], dict(H=3, Hk=2), 1),
+    ([0, 100], dict(causal=1, block_q=64, block_k=64), 2),
+    ([0, 100], dict(window=8), 1)])
+def test_varlen_rejects_bad_descriptions(lib, cu, kw, code):
+    from block_sparse_attention_fwd_gb300 import _lib
+    v, arr = _varlen(cu, **kw)
+    sz = _lib.VarlenSizes()
+    assert lib.bl_varlen_layout(ctypes.byref(v), ctypes.byref(sz)) == code
+    ok = ctypes.c_void_p(0x10000)
+    assert lib.bl_attn_fwd_varlen(ctypes.byref(v), ok, ok, ok, 0.1, ok, ok, None, None) == code
+    L = _lib.Lists(ok, ok, ok, ok, ok, None)
+    assert lib.bl_mask_from_stats_varlen(ctypes.byref(v), ok, ok, 0.05, ctypes.byref(L),
+                                         None) == code
+    assert lib.bl_attn_bwd_varlen(ctypes.byref(v), ok, ok, ok, ok, ok, ok, 0.1, None, ok, ok,
+                                  ok, ok, 1 << 30, None) == code
+    assert lib.bl_varlen_layout(None, ctypes.byref(sz)) == 1
+
+
+def test_varlen_calls_reject_bad_arguments_without_launching(lib):
+    from block_sparse_attention_fwd_gb300 import _lib
+    v, arr = _varlen([0, 100, 356])
+    sz = _lib.VarlenSizes()
+    assert lib.bl_varlen_layout(ctypes.byref(v), ctypes.byref(sz)) == 0
+    ok, odd, odd4 = (ctypes.c_void_p(x) for x in (0x10000, 0x10004, 0x10002))
+    V = ctypes.byref(v)
+    assert lib.bl_attn_fwd_varlen(V, odd, ok, ok, 0.1, ok, ok, None, None) == 1
+    assert lib.bl_attn_fwd_varlen(V, ok, ok, ok, 0.1, ok, odd4, None, None) == 1   # lse: 4 bytes
+    assert lib.bl_attn_fwd_varlen(V, ok, ok, ok, 0.0, ok, ok, None, None) == 1
+    assert lib.bl_attn_fwd_varlen(V, ok, ok, ok, 0.1, ok, ok, odd, None) == 1
+    L = _lib.Lists(ok, ok, ok, ok, ok, None)
+    for p in (-0.1, 1.0, float("nan")):
+        assert lib.bl_mask_from_stats_varlen(V, ok, ok, p, ctypes.byref(L), None) == 1
+    need = sz.bwd_workspace_bytes
+    assert lib.bl_attn_bwd_varlen(V, ok, ok, ok, ok, ok, ok, 0.1, None, ok, ok, ok, ok,
+                                  need - 1, None) == 4
+    assert lib.bl_attn_bwd_varlen(V, ok, ok, ok, ok, ok, ok, 0.1, None, ok, ok, ok, None,
+                                  need, None) == 4
+    assert lib.bl_attn_bwd_varlen(V, ok, ok, ok, ok, ok, odd4, 0.1, None, ok, ok, ok, ok,
+                                  need, None) == 1
+    assert lib.bl_varlen_bwd_check_status(V, None, None) == 4
+
+
+def test_varlen_long_sequence_limit_is_the_mask_passs_only(lib):
+    from block_sparse_attention_fwd_gb300 import _lib
+    v, arr = _varlen([0, 1000, 300000])           # T_c = 2336 > 2048 for the second
+    sz = _lib.VarlenSizes()
+    assert lib.bl_varlen_layout(ctypes.byref(v), ctypes.byref(sz)) == 0
+    ok = ctypes.c_void_p(0x10000)
+    L = _lib.Lists(ok, ok, ok, ok, ok, None)
+    assert lib.bl_mask_from_stats_varlen(ctypes.byref(v), ok, ok, 0.05, ctypes.byref(L),
+                                         None) == 2
