@@ -488,7 +488,20 @@ def run_all_configs(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     pk = _peaks()
-    names = args.configs.split(",") if args.configs else [
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    names = [x for x in args.configs.split(",") if x] if args.configs else [
         "tiny_n256_d64", "clustered_n4096_d64", "gqa_n8192_d128", "video_n32760_d128",
         "long_n131072_d128", "llm_causal_n16384_d128", "llm_window2048_n16384_d128"]
     for name in names:
@@ -503,19 +516,6 @@ def run_all_configs(args):
         lists = _lib.alloc_lists(shape, dev)
         g_q, g_k, g_v = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
         wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
-
-        def timed(fn, reps):
-            fn()
-            torch.cuda.synchronize()
-            ts = []
-            for _ in range(reps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                torch.cuda.synchronize()
-                ts.append(a.elapsed_time(b))
-            return statistics.median(ts)
 
         reps = 3 if w.n >= 100000 else 5
         fwd = timed(lambda: _lib.attn_fwd(shape, qd, kd, vd, w.scale, o, lse, stats), reps)
@@ -560,7 +560,74 @@ def run_all_configs(args):
             del op, lp, oc, lc
         del qd, kd, vd, god, o, lse, stats, lists, g_q, g_k, g_v, wsb
         torch.cuda.empty_cache()
+    packed = [x for x in args.packed.split(",") if x] if args.packed else list(inputs.PACKED)
+    for name in packed:
+        _run_packed(inputs.PACKED[name], pk, timed, dev)
     return 0
+
+
+def _packed_active_flop(mask, p, H):
+    """10*d*rows*cols summed over the kept tiles of every packed sequence."""
+    import torch
+    w, off, total = p.base, 0, 0.0
+    m = mask.to("cpu", torch.float64)
+    for n in p.lengths:
+        if n == 0:
+            continue
+        T_r, T_c = -(-n // w.block_q), -(-n // w.block_k)
+        blk = m[off:off + H * T_r * T_c].view(H, T_r, T_c)
+        off += H * T_r * T_c
+        rows = torch.full((T_r,), w.block_q, dtype=torch.float64)
+        rows[-1] = n - (T_r - 1) * w.block_q
+        cols = torch.full((T_c,), w.block_k, dtype=torch.float64)
+        cols[-1] = n - (T_c - 1) * w.block_k
+        total += float(10.0 * w.d * torch.einsum("hij,i,j->", blk, rows, cols))
+    return total
+
+
+def _run_packed(p, pk, timed, dev):
+    """One JSON line per packed variable-length workload: the three calls with
+    the runs spread over the library's side streams (default) and one after
+    another on the caller's stream (streams = 1)."""
+    import torch
+
+    from block_sparse_attention_fwd_gb300 import _lib, inputs
+    w = p.base
+    cu, q, k, v, go = inputs.generate_packed(w, p.lengths, seed=0)
+    qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
+    line = {"workload": p.name, "sequences": len(p.lengths), "total_tokens": p.total,
+            "lengths": list(p.lengths), "negl_prob": w.negl_probs[0]}
+    for streams in (0, 1):
+        vl = _lib.Varlen(cu, w.H, w.Hk, w.d, w.block_q, w.block_k, w.causal, w.window, streams)
+        o = torch.empty_like(qd)
+        lse = torch.empty(vl.sizes["lse"], dtype=torch.float32, device=dev)
+        stats = torch.empty(vl.sizes["tile_stats"], dtype=torch.float32, device=dev)
+        lists = _lib.alloc_varlen_lists(vl, dev)
+        g = [torch.empty_like(x) for x in (qd, kd, vd)]
+        ws = torch.empty(vl.sizes["bwd_workspace_bytes"], dtype=torch.uint8, device=dev)
+        negl = w.negl_probs[0]
+        fwd = timed(lambda: _lib.attn_fwd_varlen(vl, qd, kd, vd, w.scale, o, lse, stats), 5)
+        mask_ms = timed(lambda: _lib.mask_from_stats_varlen(vl, stats, lse, negl, lists), 5)
+        bwd = timed(lambda: _lib.attn_bwd_varlen(vl, qd, kd, vd, o, god, lse, w.scale, lists,
+                                                 *g, ws), 5)
+        dense = timed(lambda: _lib.attn_bwd_varlen(vl, qd, kd, vd, o, god, lse, w.scale, None,
+                                                   *g, ws), 5)
+        if _lib.varlen_bwd_check_status(vl, ws) != 0:
+            raise RuntimeError("packed backward reported a bad status")
+        tag = "" if streams == 0 else "_serial"
+        line.update({f"fwd_ms{tag}": fwd, f"mask_ms{tag}": mask_ms, f"bwd_ms{tag}": bwd,
+                     f"dense_bwd_ms{tag}": dense})
+        if streams == 0:
+            comp = _packed_active_flop(lists["mask"], p, w.H)
+            line.update({"launch_groups": vl.sizes["groups"],
+                         "fwd_frac_peak": p.dense_fwd_flop() / fwd / 1e9 / pk["bf16"],
+                         "skip_frac": 1.0 - float(lists["mask"].float().mean()),
+                         "frac_bf16_peak_computed_tiles": comp / bwd / 1e9 / pk["bf16"],
+                         "dense_bwd_frac_peak": p.dense_bwd_flop() / dense / 1e9 / pk["bf16"]})
+        del o, lse, stats, lists, g, ws
+    print(json.dumps(line), flush=True)
+    del qd, kd, vd, god
+    torch.cuda.empty_cache()
 
 
 def main():
@@ -578,6 +645,8 @@ def main():
     ap.add_argument("--ref-tiles", type=int, default=256)
     ap.add_argument("--configs", default="",
                     help="comma-separated workloads for --all-configs (default: all)")
+    ap.add_argument("--packed", default="",
+                    help="comma-separated packed workloads for --all-configs (default: all)")
     ap.add_argument("--all-configs", action="store_true",
                     help="per-workload kernel times (not the contract line)")
     args = ap.parse_args()

@@ -42,7 +42,7 @@ class VarlenStruct(ctypes.Structure):
     _fields_ = [("nseq", ctypes.c_int), ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
                 ("H", ctypes.c_int), ("Hk", ctypes.c_int), ("d", ctypes.c_int),
                 ("block_q", ctypes.c_int), ("block_k", ctypes.c_int), ("causal", ctypes.c_int),
-                ("window", ctypes.c_int)]
+                ("window", ctypes.c_int), ("streams", ctypes.c_int)]
 
 
 class VarlenSizes(ctypes.Structure):
@@ -285,13 +285,14 @@ class Varlen:
     copy of cu_seqlens (nseq + 1 int32 offsets) that the C struct points at,
     and the element counts bl_varlen_layout reports."""
 
-    def __init__(self, cu_seqlens, H, Hk, d, block_q=128, block_k=128, causal=0, window=0):
+    def __init__(self, cu_seqlens, H, Hk, d, block_q=128, block_k=128, causal=0, window=0,
+                 streams=0):
         cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist")
                                else cu_seqlens)]
         self.cu_seqlens = cu
         self._cu = (ctypes.c_int32 * len(cu))(*cu)
         self.struct = VarlenStruct(len(cu) - 1, self._cu, H, Hk, d, block_q, block_k,
-                                   int(causal), int(window))
+                                   int(causal), int(window), int(streams))
         self.H, self.Hk, self.d = H, Hk, d
         self.block_q, self.block_k = block_q, block_k
         self.causal, self.window = int(causal), int(window)

@@ -5,13 +5,22 @@
 // every buffer.  Token for token, a run of `count` sequences of length n is a
 // [count, n, heads, d] batch, and the packed layout stores each per-sequence
 // array exactly as the fixed-length call lays it out for that batch, so every
-// result equals the fixed-length call on each sequence alone.  No host wait
-// separates the launches.
+// result equals the fixed-length call on each sequence alone.
+//
+// A short sequence's launch fills only part of the 152 SMs, so the runs go
+// to a few side streams that the GPU runs side by side: largest run first,
+// each to the stream with the least work so far.  The side streams wait on
+// an event recorded on the caller's stream and the caller's stream waits on
+// one event per side stream, so the work stays ordered with the caller's and
+// the calls can be captured in a CUDA graph.  No host wait separates the
+// launches.
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
+#include <numeric>
 #include <vector>
 
 #include "../../include/bl_attn.h"
@@ -26,18 +35,35 @@ struct Run {
   bl::Shape sh;                                   // B = sequences of the run, n = their length
   int64_t tok;                                    // first token row of q/k/v/o and gradients
   size_t lse, stats, mask, kv_cnt, q_idx, q_cnt;  // element offsets of the run's blocks
+  size_t ws;                                      // byte offset of its D and dQ areas
+  double work;                                    // attending tile pairs, for scheduling
 };
 
 // Status words of the varlen backward: one 16-byte slot per run (flags word,
-// work-item counter), after the shared D and dQ areas.
+// work-item counter), after the runs' D and dQ areas.
 constexpr size_t kSlotBytes = 16;
+constexpr int kMaxStreams = 8;
+constexpr int kDefaultStreams = 4;
 
 struct Plan {
   std::vector<Run> runs;
   bl_varlen_sizes sz;
-  size_t ws_D, ws_dq;  // largest D and dQ areas over the runs
+  size_t ws_areas;     // bytes of all runs' D and dQ areas
   int max_T_c;         // most key tiles of any sequence
+  int streams;         // side streams to spread the runs over (1: the caller's only)
 };
+
+// (query tile, key tile) pairs of one sequence that hold an attending pair.
+double attending_tiles(const bl::Shape& sh) {
+  if (!sh.causal && !sh.window) return (double)sh.T_r * sh.T_c;
+  double t = 0;
+  for (int i = 0; i < sh.T_r; ++i) {
+    int lo, hi;
+    bl::key_tile_range(sh, i, lo, hi);
+    t += hi - lo + 1;
+  }
+  return t;
+}
 
 bl_status make_plan(const bl_varlen* v, Plan* p) {
   if (!v || !v->cu_seqlens || v->nseq < 1) return BL_ERR_INVALID_ARG;
@@ -46,6 +72,7 @@ bl_status make_plan(const bl_varlen* v, Plan* p) {
   for (int s = 0; s < v->nseq; ++s)
     if (cu[s + 1] < cu[s]) return BL_ERR_INVALID_ARG;
   if (cu[v->nseq] < 1) return BL_ERR_INVALID_ARG;
+  if (v->streams < 0 || v->streams > kMaxStreams) return BL_ERR_INVALID_ARG;
   // The head and tile fields follow the fixed-length rules whatever the lengths.
   const bl_shape probe = {1, 1, v->H, v->Hk, v->d, v->block_q, v->block_k, v->causal, v->window};
   bl::Shape sh;
@@ -54,7 +81,7 @@ bl_status make_plan(const bl_varlen* v, Plan* p) {
 
   p->runs.clear();
   memset(&p->sz, 0, sizeof(p->sz));
-  p->ws_D = p->ws_dq = 0;
+  p->ws_areas = 0;
   p->max_T_c = 0;
   bl_varlen_sizes& z = p->sz;
   z.total = (size_t)cu[v->nseq];
@@ -86,14 +113,83 @@ bl_status make_plan(const bl_varlen* v, Plan* p) {
     z.kv_cnt += BH * r.sh.T_r;
     z.q_idx += BH * r.sh.T_c * r.sh.T_r;
     z.q_cnt += BH * r.sh.T_c;
-    p->ws_D = std::max(p->ws_D, bl::ws_D_bytes(r.sh));
-    p->ws_dq = std::max(p->ws_dq, bl::ws_dq_bytes(r.sh));
+    r.ws = p->ws_areas;
+    p->ws_areas += bl::ws_D_bytes(r.sh) + bl::ws_dq_bytes(r.sh);
+    r.work = r.sh.B * (double)r.sh.H * attending_tiles(r.sh);
     p->runs.push_back(r);
     s = e;
   }
   z.groups = (int)p->runs.size();
-  z.bwd_workspace_bytes = p->ws_D + p->ws_dq + p->runs.size() * kSlotBytes;
+  z.bwd_workspace_bytes = p->ws_areas + p->runs.size() * kSlotBytes;
+  p->streams = std::min<int>(v->streams ? v->streams : kDefaultStreams, (int)p->runs.size());
   return BL_OK;
+}
+
+// Side streams and events of one device, created on first use and kept for
+// the life of the process.  `mu` serialises the fork/launch/join sequence of
+// a call, because the events are reused from call to call.
+struct Pool {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t side[kMaxStreams] = {};
+  cudaEvent_t fork = nullptr, join[kMaxStreams] = {};
+};
+constexpr int kMaxDevices = 64;
+Pool g_pool[kMaxDevices];
+
+cudaError_t pool_init(Pool& pl) {
+  if (pl.ready) return cudaSuccess;
+  cudaError_t e = cudaEventCreateWithFlags(&pl.fork, cudaEventDisableTiming);
+  for (int i = 0; i < kMaxStreams && e == cudaSuccess; ++i) {
+    e = cudaStreamCreateWithFlags(&pl.side[i], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl.join[i], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) pl.ready = true;
+  return e;
+}
+
+// Runs launch(run, stream) for every run of the plan: all on the caller's
+// stream when the plan uses one stream, else spread over the side streams
+// between a fork and a join on the caller's stream.  The join is enqueued
+// even when a launch fails, so the caller's stream never runs ahead of work
+// already enqueued.
+template <typename F>
+bl_status run_all(const Plan& p, cudaStream_t caller, F&& launch) {
+  if (p.streams <= 1) {
+    for (const Run& r : p.runs)
+      if (launch(r, caller) != cudaSuccess) return BL_ERR_CUDA;
+    return BL_OK;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BL_ERR_CUDA;
+  Pool& pl = g_pool[dev];
+  std::lock_guard<std::mutex> lock(pl.mu);
+  if (pool_init(pl) != cudaSuccess) return BL_ERR_CUDA;
+
+  std::vector<size_t> order(p.runs.size());
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](size_t a, size_t b) { return p.runs[a].work > p.runs[b].work; });
+  double load[kMaxStreams] = {};
+
+  cudaError_t e = cudaEventRecord(pl.fork, caller);
+  if (e != cudaSuccess) return BL_ERR_CUDA;
+  for (int i = 0; i < p.streams; ++i)
+    if (cudaStreamWaitEvent(pl.side[i], pl.fork, 0) != cudaSuccess) e = cudaErrorUnknown;
+  if (e == cudaSuccess) {
+    for (size_t idx : order) {
+      const int i = (int)(std::min_element(load, load + p.streams) - load);
+      load[i] += p.runs[idx].work;
+      if ((e = launch(p.runs[idx], pl.side[i])) != cudaSuccess) break;
+    }
+  }
+  bl_status st = e == cudaSuccess ? BL_OK : BL_ERR_CUDA;
+  for (int i = 0; i < p.streams; ++i) {
+    if (cudaEventRecord(pl.join[i], pl.side[i]) != cudaSuccess ||
+        cudaStreamWaitEvent(caller, pl.join[i], 0) != cudaSuccess)
+      st = BL_ERR_CUDA;
+  }
+  return st;
 }
 
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -111,7 +207,7 @@ __nv_bfloat16* rows(void* base, int64_t tok, int heads, int d) {
 }
 
 int32_t* status_slot(void* workspace, const Plan& p, size_t run) {
-  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + p.ws_D + p.ws_dq +
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + p.ws_areas +
                                     run * kSlotBytes);
 }
 
@@ -139,13 +235,11 @@ bl_status bl_attn_fwd_varlen(const bl_varlen* varlen, const void* q, const void*
     return BL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
   const int H = varlen->H, Hk = varlen->Hk, d = varlen->d;
-  for (const Run& r : p.runs) {
-    cudaError_t e = bl::launch_fwd(r.sh, rows(q, r.tok, H, d), rows(k, r.tok, Hk, d),
-                                   rows(v, r.tok, Hk, d), rows(o, r.tok, H, d), lse + r.lse,
-                                   at(tile_stats, r.stats), scale, (cudaStream_t)stream);
-    if (e != cudaSuccess) return BL_ERR_CUDA;
-  }
-  return BL_OK;
+  return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
+    return bl::launch_fwd(r.sh, rows(q, r.tok, H, d), rows(k, r.tok, Hk, d),
+                          rows(v, r.tok, Hk, d), rows(o, r.tok, H, d), lse + r.lse,
+                          at(tile_stats, r.stats), scale, st);
+  });
 }
 
 bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_stats,
@@ -161,15 +255,12 @@ bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_s
   if (!(negl_prob >= 0.0) || !(negl_prob < 1.0)) return BL_ERR_INVALID_ARG;
   if (p.max_T_c > 2048) return BL_ERR_UNSUPPORTED;
   const unsigned long long T = bl::mask_threshold(negl_prob);
-  for (const Run& r : p.runs) {
-    cudaError_t e = bl::launch_mask(r.sh, tile_stats + r.stats, lse + r.lse, T,
-                                    lists->mask + r.mask, lists->kv_idx + r.mask,
-                                    lists->kv_cnt + r.kv_cnt, lists->q_idx + r.q_idx,
-                                    lists->q_cnt + r.q_cnt, lists->nan_count,
-                                    (cudaStream_t)stream);
-    if (e != cudaSuccess) return BL_ERR_CUDA;
-  }
-  return BL_OK;
+  return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
+    return bl::launch_mask(r.sh, tile_stats + r.stats, lse + r.lse, T, lists->mask + r.mask,
+                           lists->kv_idx + r.mask, lists->kv_cnt + r.kv_cnt,
+                           lists->q_idx + r.q_idx, lists->q_cnt + r.q_cnt, lists->nan_count,
+                           st);
+  });
 }
 
 bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void* k,
@@ -188,19 +279,18 @@ bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void*
   if (!workspace || !bl::aligned16(workspace)) return BL_ERR_WORKSPACE;
   if (workspace_bytes < p.sz.bwd_workspace_bytes) return BL_ERR_WORKSPACE;
   const int H = varlen->H, Hk = varlen->Hk, d = varlen->d;
-  float* ws_D = static_cast<float*>(workspace);
-  float* ws_dq = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ws_D);
-  for (size_t i = 0; i < p.runs.size(); ++i) {
-    const Run& r = p.runs[i];
-    cudaError_t e = bl::launch_bwd(
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
+    float* ws_D = reinterpret_cast<float*>(ws + r.ws);
+    float* ws_dq = reinterpret_cast<float*>(ws + r.ws + bl::ws_D_bytes(r.sh));
+    const size_t idx = (size_t)(&r - p.runs.data());
+    return bl::launch_bwd(
         r.sh, rows(q, r.tok, H, d), rows(k, r.tok, Hk, d), rows(v, r.tok, Hk, d),
         rows(o, r.tok, H, d), rows(g_o, r.tok, H, d), lse + r.lse, scale,
         lists ? lists->q_idx + r.q_idx : nullptr, lists ? lists->q_cnt + r.q_cnt : nullptr,
         rows(g_q, r.tok, H, d), rows(g_k, r.tok, Hk, d), rows(g_v, r.tok, Hk, d), ws_D, ws_dq,
-        status_slot(workspace, p, i), (cudaStream_t)stream);
-    if (e != cudaSuccess) return BL_ERR_CUDA;
-  }
-  return BL_OK;
+        status_slot(workspace, p, idx), st);
+  });
 }
 
 bl_status bl_varlen_bwd_check_status(const bl_varlen* varlen, const void* workspace,

@@ -217,3 +217,58 @@ def generate_packed(w: Workload, lengths, seed: int = 0):
             parts.append([x[0] for x in generate(ws, seed=seed + s)])
     q, k, v, go = (torch.cat([p[i] for p in parts], dim=0).contiguous() for i in range(4))
     return cu, q, k, v, go
+
+
+def document_lengths(total: int, seed: int = 0, median: int = 1536, sigma: float = 1.0,
+                     lo: int = 64, hi: int = 8192):
+    """Lengths of documents packed into one batch of ``total`` tokens: log-normal
+    draws (median ``median``, shape ``sigma``) clipped to [lo, hi], the last
+    one cut so that the lengths add up to ``total``."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    left = total
+    while left > 0:
+        n = int(np.clip(round(median * math.exp(sigma * rng.standard_normal())), lo, hi))
+        n = min(n, left)
+        out.append(n)
+        left -= n
+    return out
+
+
+@dataclasses.dataclass(frozen=True)
+class Packed:
+    """A packed variable-length batch: the per-sequence recipe of ``base`` (its
+    B and n are ignored) and the sequence lengths."""
+    name: str
+    base: Workload
+    lengths: tuple
+
+    @property
+    def total(self) -> int:
+        return sum(self.lengths)
+
+    def seq(self, n: int) -> Workload:
+        return dataclasses.replace(self.base, B=1, n=n)
+
+    def dense_fwd_flop(self) -> float:
+        return sum(self.seq(n).dense_fwd_flop() for n in self.lengths if n)
+
+    def dense_bwd_flop(self) -> float:
+        return sum(self.seq(n).dense_bwd_flop() for n in self.lengths if n)
+
+
+PACKED = {
+    # decoder pre-training batch: 16384 tokens of documents of mixed length
+    "llm_packed_causal_t16384_d128": Packed(
+        "llm_packed_causal_t16384_d128",
+        Workload("doc", B=1, n=1, H=32, Hk=8, d=128, block_q=128, block_k=128,
+                 negl_probs=(0.05,), kind="runs", alpha=3.0, run=64, clusters=64,
+                 causal=True),
+        tuple(document_lengths(16384, seed=0))),
+    # four equal video clips of the 32760-token grid's 1-D stand-in: one launch group
+    "video_packed_4x8190_d128": Packed(
+        "video_packed_4x8190_d128",
+        Workload("clip", B=1, n=1, H=40, Hk=40, d=128, block_q=128, block_k=128,
+                 negl_probs=(0.05,), kind="runs", alpha=3.0, run=128, clusters=64),
+        (8190, 8190, 8190, 8190)),
+}

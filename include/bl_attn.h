@@ -236,21 +236,29 @@ bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* 
  *
  * Execution: the calls walk the sequences on the host and run the
  * fixed-length kernels once per run of consecutive sequences of equal
- * length (such a run is exactly a [count, n_s, ...] batch).  Nothing waits
- * on the host between launches, so the calls can be captured in a CUDA
- * graph.  lse only needs 4-byte alignment here; the other device pointers
- * need 16 bytes, as in the fixed-length calls.
+ * length (such a run is exactly a [count, n_s, ...] batch).  The runs are
+ * spread over up to `streams` side streams of the library (largest run
+ * first, each to the least-loaded stream), forked from and joined back to
+ * the caller's stream with events, so that short sequences fill the GPU
+ * together; the call returns with all its work ordered before anything the
+ * caller enqueues next on its stream.  Nothing waits on the host, so the
+ * calls can be captured in a CUDA graph.  lse only needs 4-byte alignment
+ * here; the other device pointers need 16 bytes, as in the fixed-length
+ * calls.
  * ------------------------------------------------------------------------- */
 
 /* cu_seqlens: HOST array of nseq + 1 int32, cu_seqlens[0] = 0,
- * non-decreasing, cu_seqlens[nseq] >= 1.  The other fields mean what they
- * mean in bl_shape and obey the same limits. */
+ * non-decreasing, cu_seqlens[nseq] >= 1.  streams: most runs in flight at
+ * once, 1..8, or 0 for the default of 4; 1 runs them one after another on
+ * the caller's stream.  The other fields mean what they mean in bl_shape and
+ * obey the same limits. */
 typedef struct {
   int nseq;
   const int32_t* cu_seqlens;
   int H, Hk, d;
   int block_q, block_k;
   int causal, window;
+  int streams;
 } bl_varlen;
 
 /* Element counts (bytes for bwd_workspace_bytes) of a packed batch. */
@@ -283,8 +291,8 @@ bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_s
                                     const bl_lists* lists, void* stream);
 
 /* bl_attn_bwd over a packed batch.  workspace: at least
- * sizes.bwd_workspace_bytes; runs of sequences reuse its D and dQ areas one
- * after another on the stream and each has its own status word. */
+ * sizes.bwd_workspace_bytes; every run has its own D and dQ areas and status
+ * word in it. */
 bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void* k,
                              const void* v, const void* o, const void* g_o,
                              const float* lse, float scale, const bl_lists* lists,

@@ -143,11 +143,11 @@ def test_grad_error_rejects_bad_arguments(lib):
 
 def _varlen(cu, **kw):
     from block_sparse_attention_fwd_gb300 import _lib
-    a = dict(H=4, Hk=2, d=64, block_q=128, block_k=128, causal=0, window=0)
+    a = dict(H=4, Hk=2, d=64, block_q=128, block_k=128, causal=0, window=0, streams=0)
     a.update(kw)
     arr = (ctypes.c_int32 * len(cu))(*cu)
     v = _lib.VarlenStruct(len(cu) - 1, arr, a["H"], a["Hk"], a["d"], a["block_q"],
-                          a["block_k"], a["causal"], a["window"])
+                          a["block_k"], a["causal"], a["window"], a["streams"])
     return v, arr
 
 
@@ -169,7 +169,15 @@ def test_varlen_layout_matches_the_oracle_layout(lib, cu, bq, bk):
     # one launch group per run of equal non-zero lengths
     lens = [b - a for a, b in zip(cu[:-1], cu[1:]) if b > a]
     assert sz.groups == sum(1 for i, n in enumerate(lens) if i == 0 or lens[i - 1] != n)
-    assert sz.bwd_workspace_bytes >= max(4 * 4 * 64 * n for n in lens)
+    # every run has its own D [B,H,n] and dQ [B,n,H,d] fp32 areas and a status slot
+    runs = []
+    for i, n in enumerate(lens):
+        if i and lens[i - 1] == n:
+            runs[-1][0] += 1
+        else:
+            runs.append([1, n])
+    want = sum(-(-(b * 4 * n * 4) // 256) * 256 + b * n * 4 * 64 * 4 for b, n in runs)
+    assert sz.bwd_workspace_bytes == want + 16 * len(runs)
 
 
 @pytest.mark.parametrize("cu,kw,code", [
@@ -180,7 +188,9 @@ def test_varlen_layout_matches_the_oracle_layout(lib, cu, bq, bk):
     ([0, 100], dict(d=96), 2),
     ([0, 100], dict(H=3, Hk=2), 1),
     ([0, 100], dict(causal=1, block_q=64, block_k=64), 2),
-    ([0, 100], dict(window=8), 1)])
+    ([0, 100], dict(window=8), 1),
+    ([0, 100], dict(streams=-1), 1),
+    ([0, 100], dict(streams=9), 1)])
 def test_varlen_rejects_bad_descriptions(lib, cu, kw, code):
     from block_sparse_attention_fwd_gb300 import _lib
     v, arr = _varlen(cu, **kw)

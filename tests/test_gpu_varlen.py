@@ -35,14 +35,14 @@ def built():
     g.build()
 
 
-def _setup(cfg, lengths, seed=0):
+def _setup(cfg, lengths, seed=0, streams=0):
     from block_sparse_attention_fwd_gb300 import _lib
     w = inputs.custom("packed", B=1, n=1, H=cfg["H"], Hk=cfg["Hk"], d=cfg["d"],
                       block_q=cfg["block"], block_k=cfg["block"], run=32, clusters=6,
                       causal=cfg["causal"], window=cfg["window"])
     cu, q, k, v, go = inputs.generate_packed(w, lengths, seed=seed)
     vl = _lib.Varlen(cu, cfg["H"], cfg["Hk"], cfg["d"], cfg["block"], cfg["block"],
-                     cfg["causal"], cfg["window"])
+                     cfg["causal"], cfg["window"], streams)
     return w, cu, q, k, v, go, vl
 
 
@@ -195,3 +195,35 @@ def test_varlen_autograd_module_matches_torch():
     for a, b in ((k, kf), (v, vf)):
         want = b.grad[0].transpose(0, 1).reshape(T, Hk, H // Hk, d).sum(2)
         assert U.rel_l2(U.cpu(a.grad), want.cpu().numpy()) <= U.REL_L2
+
+
+def test_varlen_concurrent_runs_match_serial_runs():
+    """Runs spread over side streams give the same forward, statistics and
+    lists, bit for bit, as runs one after another on the caller's stream, and
+    the same gradients up to the order of the dQ reduce-adds; a later kernel
+    on the caller's stream sees every run's output (the join)."""
+    from block_sparse_attention_fwd_gb300 import _lib
+    cfg = dict(H=4, Hk=2, d=128, block=128, causal=True, window=0)
+    lengths = [900, 130, 2000, 1, 640, 640, 256, 1500]
+    res = {}
+    for streams in (1, 2, 8):
+        w, cu, q, k, v, go, vl = _setup(cfg, lengths, seed=6, streams=streams)
+        scale = 128 ** -0.5
+        qd, kd, vd, o, lse, stats = _gpu_forward(vl, q, k, v, scale)
+        lists = _lib.alloc_varlen_lists(vl, qd.device)
+        _lib.mask_from_stats_varlen(vl, stats, lse, 0.05, lists)
+        ws = torch.empty(vl.sizes["bwd_workspace_bytes"], dtype=torch.uint8, device="cuda")
+        g = [torch.empty_like(x) for x in (qd, kd, vd)]
+        _lib.attn_bwd_varlen(vl, qd, kd, vd, o, go.to("cuda"), lse, scale, lists, *g, ws)
+        sums = torch.stack([x.float().abs().sum() for x in g])   # on the caller's stream
+        assert _lib.varlen_bwd_check_status(vl, ws) == 0
+        res[streams] = (o, lse, stats, lists, g, sums)
+    o1, l1, s1, li1, g1, sum1 = res[1]
+    for streams in (2, 8):
+        o, lse, stats, lists, g, sums = res[streams]
+        assert torch.equal(o, o1) and torch.equal(lse, l1) and torch.equal(stats, s1)
+        for key in ("mask", "kv_idx", "kv_cnt", "q_idx", "q_cnt"):
+            assert torch.equal(lists[key], li1[key]), key
+        assert torch.equal(g[1], g1[1]) and torch.equal(g[2], g1[2])   # dK, dV: one writer
+        assert U.rel_l2(U.cpu(g[0]), U.cpu(g1[0])) <= 1e-3
+        assert torch.allclose(sums, sum1, rtol=1e-3)
