@@ -190,7 +190,8 @@ template <int D, bool MASKED>
 __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-    const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse,
+    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_gk,
+    const __grid_constant__ CUtensorMap tm_gv, const float* __restrict__ lse,
     const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
     const int32_t* __restrict__ q_cnt, __nv_bfloat16* __restrict__ g_k,
     __nv_bfloat16* __restrict__ g_v, int32_t* __restrict__ status, Shape sh, float scale,
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
   __shared__ int s_item[2];        // item of each list buffer, -1: no more items
   __shared__ int s_drain_ok[4];
   __shared__ int s_copy_ok[2];
+  __shared__ int s_ep_ok[8];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = sh.H / sh.Hk;
@@ -237,6 +239,8 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_g);
     prefetch_tmap(&tm_dq);
+    prefetch_tmap(&tm_gk);
+    prefetch_tmap(&tm_gv);
   }
   if (warp == 1) tmem_alloc(&s_tmem, C::T_COLS);
   fence_before_sync();
@@ -646,43 +650,78 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       // epilogue: warps 4-7 write dV, warps 8-11 s dK, this key tile's rows (0
       // for an item without tiles).  The accumulators are read before this
       // warpgroup's first arrival of the next item, which gates the next
-      // item's first dV and dK (they overwrite).
+      // item's first dV and dK (they overwrite).  The rows leave through the
+      // warpgroup's half of the dS^T buffer and one TMA store per 64 columns:
+      // row-per-thread global stores would touch 32 rows 10 KB apart per warp
+      // instruction and hold the SM's load/store path for thousands of
+      // cycles.  The buffer is free once the item's last dQ has completed
+      // (dq_ready), and it is rewritten only by this warpgroup's next second
+      // phase, after the stores have read it.
+      const Item ie = item_of(sh, s_item[buf]);
       if (nt > 0) {
-        ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.acc_full, kk & 1));
+        const bool mine = !failed(&s_fail) && mbar_wait(&bars.acc_full, kk & 1) &&
+                          mbar_wait(&bars.dq_ready, (t - 1) & 1);
+        // the warpgroup agrees before its named barriers
+        const bool w_ok = __all_sync(0xffffffffu, mine);
+        if (lane == 0) s_ep_ok[half * 4 + q4] = w_ok;
+        named_sync(3 + half, 128);
+        ok = s_ep_ok[half * 4] && s_ep_ok[half * 4 + 1] && s_ep_ok[half * 4 + 2] &&
+             s_ep_ok[half * 4 + 3];
+        named_sync(3 + half, 128);
         if (!ok) break;
         fence_after_sync();
         ++kk;
-      }
-      const float mul = half == 0 ? 1.f : scale;
-      const uint32_t col = half == 0 ? C::T_DV : C::T_DK;
-      const Item ie = item_of(sh, s_item[buf]);
-      const int row = ie.j * 128 + r;
-      uint4* dst = reinterpret_cast<uint4*>(
-          (half == 0 ? g_v : g_k) + (((int64_t)ie.b * sh.n + row) * sh.Hk + ie.hk) * D);
-      if (nt > 0) {   // warp-uniform: the TMEM loads are warp-collective
+        const float mul = half == 0 ? 1.f : scale;
+        const uint32_t col = half == 0 ? C::T_DV : C::T_DK;
+        uint8_t* stage = sm + C::OFF_DS + half * C::CHUNK;
+        uint8_t* srow = stage + r * 128;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t a[32];
-          tmem_ld32(lane_base + col + c0, a);
-          tmem_ld_wait();
-          if (row < sh.n) {
+        for (int hc = 0; hc < C::CHK; ++hc) {       // 64 columns = one 128-byte row
+          if (hc > 0) {                               // the previous store has read the rows
+            if (r == 0) bulk_wait_read0();
+            named_sync(3 + half, 128);
+          }
 #pragma unroll
-            for (int x8 = 0; x8 < 32; x8 += 8)
-              dst[(c0 + x8) / 8] = make_uint4(
-                  pack_bf16(__uint_as_float(a[x8]) * mul, __uint_as_float(a[x8 + 1]) * mul),
-                  pack_bf16(__uint_as_float(a[x8 + 2]) * mul, __uint_as_float(a[x8 + 3]) * mul),
-                  pack_bf16(__uint_as_float(a[x8 + 4]) * mul, __uint_as_float(a[x8 + 5]) * mul),
-                  pack_bf16(__uint_as_float(a[x8 + 6]) * mul, __uint_as_float(a[x8 + 7]) * mul));
+          for (int c32 = 0; c32 < 2; ++c32) {
+            uint32_t a[32];
+            tmem_ld32(lane_base + col + hc * 64 + c32 * 32, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x8 = 0; x8 < 4; ++x8) {
+              const int chunk = c32 * 4 + x8;
+              *reinterpret_cast<uint4*>(srow + ((chunk ^ (r & 7)) << 4)) = make_uint4(
+                  pack_bf16(__uint_as_float(a[8 * x8]) * mul, __uint_as_float(a[8 * x8 + 1]) * mul),
+                  pack_bf16(__uint_as_float(a[8 * x8 + 2]) * mul,
+                            __uint_as_float(a[8 * x8 + 3]) * mul),
+                  pack_bf16(__uint_as_float(a[8 * x8 + 4]) * mul,
+                            __uint_as_float(a[8 * x8 + 5]) * mul),
+                  pack_bf16(__uint_as_float(a[8 * x8 + 6]) * mul,
+                            __uint_as_float(a[8 * x8 + 7]) * mul));
+            }
+          }
+          fence_async_smem();
+          named_sync(3 + half, 128);
+          if (r == 0) {
+            tma_store_4d(half == 0 ? &tm_gv : &tm_gk, stage, hc * 64, ie.hk, ie.j * 128, ie.b);
+            bulk_commit();
           }
         }
-      } else if (row < sh.n) {
+        if (r == 0) bulk_wait_read0();
+        named_sync(3 + half, 128);                   // the next dS^T may overwrite the rows
+      } else {
+        const int row = ie.j * 128 + r;
+        uint4* dst = reinterpret_cast<uint4*>(
+            (half == 0 ? g_v : g_k) + (((int64_t)ie.b * sh.n + row) * sh.Hk + ie.hk) * D);
+        if (row < sh.n) {
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.list_empty[buf]);
     }
+    if (r == 0) bulk_wait0();   // the rows of the last item have been written
     if (!ok && lane == 0) fail();
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
@@ -771,11 +810,13 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
                      const int32_t* q_cnt, void* g_k, void* g_v, float* dq_acc, int32_t* status,
                      float scale, cudaStream_t st) {
   using C = Cfg<D>;
-  CUtensorMap mq, mk, mv, mg, md;
+  CUtensorMap mq, mk, mv, mg, md, mgk, mgv;
   if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
       !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 128) ||
       !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) ||
       !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
+      !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 128) ||
+      !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 128) ||
       !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
@@ -784,7 +825,8 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)sh.T_c * sh.Hk * sh.B;
   const int grid = (int)(items < sm_count() ? items : sm_count());
-  kern<<<grid, 512, smem, st>>>(mq, mk, mv, mg, md, lse, Dv, q_idx, q_cnt, (__nv_bfloat16*)g_k,
+  kern<<<grid, 512, smem, st>>>(mq, mk, mv, mg, md, mgk, mgv, lse, Dv, q_idx, q_cnt,
+                                (__nv_bfloat16*)g_k,
                                 (__nv_bfloat16*)g_v, status, sh, scale, scale * kLog2e);
   return cudaGetLastError();
 }
