@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
   __shared__ int s_item[2];        // item of each list buffer, -1: no more items
   __shared__ int s_drain_ok[4];
   __shared__ int s_copy_ok[2];
-  __shared__ int s_ep_ok[8];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = sh.H / sh.Hk;
@@ -541,6 +540,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     uint8_t* ds_row = sm + C::OFF_DS + half * C::CHUNK + r * 128;
     int t = 0, kk = 0;
     bool ok = true;
+    bool store_pending = false;   // this warp's dK/dV rows may still be read from ds_row
     for (int k = 0; ok; ++k) {
       const int buf = k & 1;
       ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
@@ -609,6 +609,11 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, t & 1));
         if (!ok) break;
         fence_after_sync();
+        if (store_pending) {                       // the rows are about to be overwritten
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          store_pending = false;
+        }
 #pragma unroll
         for (int pass = 0; pass < 4; ++pass) {    // 16 query columns per pass
           uint32_t pv[16];
@@ -650,36 +655,30 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       // epilogue: warps 4-7 write dV, warps 8-11 s dK, this key tile's rows (0
       // for an item without tiles).  The accumulators are read before this
       // warpgroup's first arrival of the next item, which gates the next
-      // item's first dV and dK (they overwrite).  The rows leave through the
-      // warpgroup's half of the dS^T buffer and one TMA store per 64 columns:
-      // row-per-thread global stores would touch 32 rows 10 KB apart per warp
-      // instruction and hold the SM's load/store path for thousands of
-      // cycles.  The buffer is free once the item's last dQ has completed
-      // (dq_ready), and it is rewritten only by this warpgroup's next second
-      // phase, after the stores have read it.
+      // item's first dV and dK (they overwrite).  Each warp stages its 32 rows
+      // in its part of the warpgroup's half of the dS^T buffer and writes them
+      // with one TMA store per 64 columns: row-per-thread global stores would
+      // touch 32 rows 10 KB apart per warp instruction and hold the SM's
+      // load/store path for thousands of cycles.  The buffer is free once the
+      // item's last dQ has completed (dq_ready); the warp waits for its
+      // stores to have read it only before it next writes dS^T there.
       const Item ie = item_of(sh, s_item[buf]);
       if (nt > 0) {
-        const bool mine = !failed(&s_fail) && mbar_wait(&bars.acc_full, kk & 1) &&
-                          mbar_wait(&bars.dq_ready, (t - 1) & 1);
-        // the warpgroup agrees before its named barriers
-        const bool w_ok = __all_sync(0xffffffffu, mine);
-        if (lane == 0) s_ep_ok[half * 4 + q4] = w_ok;
-        named_sync(3 + half, 128);
-        ok = s_ep_ok[half * 4] && s_ep_ok[half * 4 + 1] && s_ep_ok[half * 4 + 2] &&
-             s_ep_ok[half * 4 + 3];
-        named_sync(3 + half, 128);
+        ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.acc_full, kk & 1) &&
+                                         mbar_wait(&bars.dq_ready, (t - 1) & 1));
         if (!ok) break;
         fence_after_sync();
         ++kk;
         const float mul = half == 0 ? 1.f : scale;
         const uint32_t col = half == 0 ? C::T_DV : C::T_DK;
-        uint8_t* stage = sm + C::OFF_DS + half * C::CHUNK;
-        uint8_t* srow = stage + r * 128;
+        uint8_t* wstage = sm + C::OFF_DS + half * C::CHUNK + q4 * 32 * 128;   // 1024-aligned
+        uint8_t* srow = wstage + lane * 128;
+        const int row0 = ie.j * 128 + q4 * 32;
 #pragma unroll
         for (int hc = 0; hc < C::CHK; ++hc) {       // 64 columns = one 128-byte row
           if (hc > 0) {                               // the previous store has read the rows
-            if (r == 0) bulk_wait_read0();
-            named_sync(3 + half, 128);
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
           }
 #pragma unroll
           for (int c32 = 0; c32 < 2; ++c32) {
@@ -689,7 +688,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
 #pragma unroll
             for (int x8 = 0; x8 < 4; ++x8) {
               const int chunk = c32 * 4 + x8;
-              *reinterpret_cast<uint4*>(srow + ((chunk ^ (r & 7)) << 4)) = make_uint4(
+              *reinterpret_cast<uint4*>(srow + ((chunk ^ (lane & 7)) << 4)) = make_uint4(
                   pack_bf16(__uint_as_float(a[8 * x8]) * mul, __uint_as_float(a[8 * x8 + 1]) * mul),
                   pack_bf16(__uint_as_float(a[8 * x8 + 2]) * mul,
                             __uint_as_float(a[8 * x8 + 3]) * mul),
@@ -700,14 +699,13 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             }
           }
           fence_async_smem();
-          named_sync(3 + half, 128);
-          if (r == 0) {
-            tma_store_4d(half == 0 ? &tm_gv : &tm_gk, stage, hc * 64, ie.hk, ie.j * 128, ie.b);
+          __syncwarp();
+          if (lane == 0 && row0 < sh.n) {
+            tma_store_4d(half == 0 ? &tm_gv : &tm_gk, wstage, hc * 64, ie.hk, row0, ie.b);
             bulk_commit();
           }
         }
-        if (r == 0) bulk_wait_read0();
-        named_sync(3 + half, 128);                   // the next dS^T may overwrite the rows
+        store_pending = true;
       } else {
         const int row = ie.j * 128 + r;
         uint4* dst = reinterpret_cast<uint4*>(
@@ -721,7 +719,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.list_empty[buf]);
     }
-    if (r == 0) bulk_wait0();   // the rows of the last item have been written
+    if (lane == 0) bulk_wait0();   // the rows of the last item have been written
     if (!ok && lane == 0) fail();
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
@@ -815,8 +813,8 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
       !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 128) ||
       !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) ||
       !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
-      !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 128) ||
-      !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 128) ||
+      !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 32) ||
+      !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 32) ||
       !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
