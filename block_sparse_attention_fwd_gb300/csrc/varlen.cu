@@ -43,7 +43,7 @@ struct Run {
 // work-item counter), after the runs' D and dQ areas.
 constexpr size_t kSlotBytes = 16;
 constexpr int kMaxStreams = 8;
-constexpr int kDefaultStreams = 4;
+constexpr int kDefaultStreams = 8;
 
 struct Plan {
   std::vector<Run> runs;

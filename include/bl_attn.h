@@ -249,7 +249,7 @@ bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* 
 
 /* cu_seqlens: HOST array of nseq + 1 int32, cu_seqlens[0] = 0,
  * non-decreasing, cu_seqlens[nseq] >= 1.  streams: most runs in flight at
- * once, 1..8, or 0 for the default of 4; 1 runs them one after another on
+ * once, 1..8, or 0 for the default of 8; 1 runs them one after another on
  * the caller's stream.  The other fields mean what they mean in bl_shape and
  * obey the same limits. */
 typedef struct {
