@@ -357,10 +357,11 @@ def run_ours(args):
         # the metric's own kernel: the block-sparse backward on computed tiles
         "roofline_bwd": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16"],
                          "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16"],
-                         "traffic": traffic.get("bwd_tc_kernel"),
+                         "traffic": _sum_or_none(traffic, ("bwd_pre_kernel", "bwd_tc_kernel",
+                                                           "dq_convert_kernel")),
                          "kernel": "bl_attn_bwd call (D pass, which also zeroes the dQ "
                                    "accumulator, + bwd_tc_kernel + dQ convert), 10*d*valid rows*"
-                                   "valid keys per kept tile",
+                                   "valid keys per kept tile; traffic summed over the three",
                          "peak_src": pk["src"] + " burst"},
         "roofline_mask": {"bound": "hbm",
                           "achieved": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
