@@ -27,3 +27,43 @@ def max_over_ranks(value: float, device=None) -> float:
     t = torch.tensor([float(value)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def sequence_work(n: int, causal: bool = False, window: int = 0) -> int:
+    """(query, key) pairs of one sequence of length n that attend: the work of
+    its forward and backward up to a constant."""
+    if not causal:
+        return n * n
+    if not window or window >= n:
+        return n * (n + 1) // 2
+    return window * (window + 1) // 2 + (n - window) * window
+
+
+def shard_sequences(cu_seqlens, rank: int, world: int, causal: bool = False, window: int = 0):
+    """The sequences of a packed batch that rank `rank` of `world` owns.
+
+    Sequences carry no exchange either: each attends only to itself.  They go,
+    largest work first (ties by index), to the rank with the least work so far
+    (ties to the lower rank), so every rank derives the same assignment from
+    cu_seqlens alone and each sequence has exactly one owner.  Returns
+    (seq_ids ascending, local cu_seqlens of the owned sequences packed in that
+    order, their token ranges [(start, end)] in the global packing)."""
+    if world < 1 or not (0 <= rank < world):
+        raise ValueError("bad rank/world")
+    cu = [int(x) for x in cu_seqlens]
+    if not cu or cu[0] != 0 or any(b < a for a, b in zip(cu[:-1], cu[1:])):
+        raise ValueError("cu_seqlens must start at 0 and be non-decreasing")
+    lengths = [b - a for a, b in zip(cu[:-1], cu[1:])]
+    order = sorted(range(len(lengths)),
+                   key=lambda s: (-sequence_work(lengths[s], causal, window), s))
+    load = [0] * world
+    owner = [0] * len(lengths)
+    for s in order:
+        r = min(range(world), key=lambda x: (load[x], x))
+        owner[s] = r
+        load[r] += sequence_work(lengths[s], causal, window)
+    mine = [s for s in range(len(lengths)) if owner[s] == rank]
+    local = [0]
+    for s in mine:
+        local.append(local[-1] + lengths[s])
+    return mine, local, [(cu[s], cu[s + 1]) for s in mine]
