@@ -436,7 +436,9 @@ def _active_flop(mask, w):
 
 def _e2e(args, w, shape, q, k, v, go, negl, dev):
     """Same step through the public API with host buffers: pinned H2D copies of
-    Q, K, V, G_O and D2H copies of G_Q, G_K, G_V inside the timed region."""
+    Q, K, V, G_O and D2H copies of G_Q, G_K, G_V inside the timed region.  G_O
+    is needed only by the backward, so it uploads on a copy stream while the
+    forward and the mask run; everything else is ordered on one stream."""
     import torch
 
     from block_sparse_attention_fwd_gb300 import _lib
@@ -451,12 +453,19 @@ def _e2e(args, w, shape, q, k, v, go, negl, dev):
     gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
     wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    go_ready = torch.cuda.Event()
 
     def one():
-        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dg, hg)):
+        copy.wait_stream(stream)                   # the previous step's backward read dg
+        with torch.cuda.stream(copy):
+            dg.copy_(hg, non_blocking=True)
+            go_ready.record(copy)
+        for dst, src in ((dq, hq), (dk, hk), (dv, hv)):
             dst.copy_(src, non_blocking=True)
         _lib.attn_fwd(shape, dq, dk, dv, w.scale, o, lse, stats)
         _lib.mask_from_stats(shape, stats, lse, negl, lists)
+        stream.wait_event(go_ready)
         _lib.attn_bwd(shape, dq, dk, dv, o, dg, lse, w.scale, lists, gq, gk, gv, wsb)
         for dst, src in zip(outs, (gq, gk, gv)):
             dst.copy_(src, non_blocking=True)
