@@ -239,3 +239,60 @@ def test_varlen_long_sequence_limit_is_the_mask_passs_only(lib):
     L = _lib.Lists(ok, ok, ok, ok, ok, None)
     assert lib.bl_mask_from_stats_varlen(ctypes.byref(v), ok, ok, 0.05, ctypes.byref(L),
                                          None) == 2
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "bl_attn.h"
+
+int main(void) {
+  bl_shape s = {1, 1000, 2, 1, 64, 128, 64, 0, 0};
+  int32_t cu[4] = {0, 100, 100, 356};
+  bl_varlen v;
+  bl_varlen_sizes z;
+  bl_status st;
+  printf("%zu %zu\n", bl_tile_stats_elems(&s), bl_bwd_workspace_bytes(&s));
+  memset(&v, 0, sizeof v);
+  v.nseq = 3; v.cu_seqlens = cu; v.H = 4; v.Hk = 2; v.d = 64; v.block_q = 128; v.block_k = 128;
+  st = bl_varlen_layout(&v, &z);
+  printf("%d %zu %zu %zu %zu %zu %zu %zu %zu %d\n", (int)st, z.total, z.lse, z.tile_stats, z.mask,
+         z.kv_cnt, z.q_idx, z.q_cnt, z.bwd_workspace_bytes, z.groups);
+  printf("%d\n", (int)bl_attn_fwd(&s, NULL, NULL, NULL, 0.125f, NULL, NULL, NULL, NULL));
+  printf("%s\n", bl_status_string(BL_ERR_UNSUPPORTED));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """The header compiles as C99 with warnings as errors, and a C program
+    linked against the library gets the same sizes as the Python binding
+    (host-side calls only: nothing reaches a GPU)."""
+    import subprocess
+    from block_sparse_attention_fwd_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", libdir, "-lbl_attn", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.strip().splitlines()
+    s = _shape(n=1000, H=2, Hk=1, d=64, block_q=128, block_k=64)
+    assert lines[0].split() == [str(_lib.tile_stats_elems(s)), str(_lib.bwd_workspace_bytes(s))]
+    vl = _lib.Varlen([0, 100, 100, 356], 4, 2, 64, 128, 128)
+    z = vl.sizes
+    want = [0, z["total"], z["lse"], z["tile_stats"], z["mask"], z["kv_cnt"], z["q_idx"],
+            z["q_cnt"], z["bwd_workspace_bytes"], z["groups"]]
+    assert [int(x) for x in lines[1].split()] == want
+    assert want[1:4] == [356, 4 * 356, 4 * 1 * 128 + 4 * 2 * 256] and want[-1] == 2
+    assert lines[2] == "1"                           # BL_ERR_INVALID_ARG before any launch
+    assert lines[3] == "unsupported configuration"
