@@ -296,3 +296,20 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     assert want[1:4] == [356, 4 * 356, 4 * 1 * 128 + 4 * 2 * 256] and want[-1] == 2
     assert lines[2] == "1"                           # BL_ERR_INVALID_ARG before any launch
     assert lines[3] == "unsupported configuration"
+
+
+def test_varlen_splits_runs_longer_than_the_grid_limit(lib):
+    """70000 sequences of one token: a launch group holds at most 65535
+    sequences (the grid's batch dimension), so the run splits in two; the
+    sizes are still the sum over sequences."""
+    from block_sparse_attention_fwd_gb300 import _lib
+    cu = list(range(70001))
+    v, arr = _varlen(cu, H=2, Hk=1, d=64, block_q=64, block_k=64)
+    sz = _lib.VarlenSizes()
+    assert lib.bl_varlen_layout(ctypes.byref(v), ctypes.byref(sz)) == 0
+    assert sz.groups == 2
+    assert (sz.total, sz.lse, sz.tile_stats, sz.mask, sz.kv_cnt) == \
+        (70000, 2 * 70000, 2 * 64 * 70000, 2 * 70000, 2 * 70000)
+    # one D area (256-byte rounded) and one dQ area per group, one 16-byte slot each
+    want = sum(-(-(b * 2 * 4) // 256) * 256 + b * 2 * 64 * 4 for b in (65535, 4465)) + 2 * 16
+    assert sz.bwd_workspace_bytes == want
