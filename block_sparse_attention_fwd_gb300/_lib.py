@@ -19,7 +19,7 @@ BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "B
              4: "BL_ERR_WORKSPACE", 5: "BL_ERR_CORRUPT_LISTS", 6: "BL_ERR_TIMEOUT"}
 
 # Every symbol include/bl_attn.h declares (checked by the CPU test suite).
-EXPORTS = ("bl_tile_stats_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
+EXPORTS = ("bl_tile_stats_elems", "bl_lists_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
            "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
            "bl_attn_bwd_noalloc", "bl_lse_combine", "bl_grad_error", "bl_varlen_layout",
            "bl_attn_fwd_varlen", "bl_mask_from_stats_varlen", "bl_attn_bwd_varlen",
@@ -75,6 +75,8 @@ def load():
     P, S, F, D, Z = ctypes.c_void_p, ctypes.POINTER(Shape), ctypes.c_float, ctypes.c_double, ctypes.c_size_t
     lib.bl_tile_stats_elems.argtypes = [S]
     lib.bl_tile_stats_elems.restype = Z
+    lib.bl_lists_elems.argtypes = [S, ctypes.POINTER(ctypes.c_size_t)]
+    lib.bl_lists_elems.restype = Z
     lib.bl_bwd_workspace_bytes.argtypes = [S]
     lib.bl_bwd_workspace_bytes.restype = Z
     lib.bl_attn_fwd.argtypes = [S, P, P, P, F, P, P, P, P]
@@ -145,6 +147,13 @@ def tiles(shape: Shape):
 
 def tile_stats_elems(shape: Shape) -> int:
     return int(load().bl_tile_stats_elems(ctypes.byref(shape)))
+
+
+def lists_elems(shape: Shape):
+    """(element counts of mask, kv_idx, kv_cnt, q_idx, q_cnt, total bytes)."""
+    out = (ctypes.c_size_t * 5)()
+    total = int(load().bl_lists_elems(ctypes.byref(shape), out))
+    return tuple(int(x) for x in out) + (total,)
 
 
 def bwd_workspace_bytes(shape: Shape) -> int:

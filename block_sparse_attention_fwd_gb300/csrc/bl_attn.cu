@@ -54,6 +54,17 @@ size_t bl_tile_stats_elems(const bl_shape* shape) {
   return (size_t)sh.B * sh.H * sh.T_c * (size_t)sh.n_pad;
 }
 
+size_t bl_lists_elems(const bl_shape* shape, size_t out[5]) {
+  bl::Shape sh;
+  if (!out || check_shape(shape, &sh) != BL_OK) return 0;
+  const size_t bh = (size_t)sh.B * sh.H;
+  out[0] = out[1] = bh * sh.T_r * sh.T_c;
+  out[2] = bh * sh.T_r;
+  out[3] = bh * sh.T_c * sh.T_r;
+  out[4] = bh * sh.T_c;
+  return out[0] + 4 * (out[1] + out[2] + out[3] + out[4]);
+}
+
 size_t bl_bwd_workspace_bytes(const bl_shape* shape) {
   bl::Shape sh;
   if (check_shape(shape, &sh) != BL_OK) return 0;

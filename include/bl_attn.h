@@ -93,6 +93,12 @@ typedef struct {
 /* Number of fp32 elements of tile_stats: B*H*T_c*T_r*block_q. */
 size_t bl_tile_stats_elems(const bl_shape* shape);
 
+/* Element counts of the five list arrays of bl_lists, written to out[0..4]
+ * in field order: mask and kv_idx B*H*T_r*T_c each, kv_cnt B*H*T_r, q_idx
+ * B*H*T_c*T_r, q_cnt B*H*T_c.  Returns the total bytes of the five arrays
+ * (uint8 mask, int32 others), or 0 for an invalid shape (out untouched). */
+size_t bl_lists_elems(const bl_shape* shape, size_t out[5]);
+
 /* Bytes of device workspace bl_attn_bwd needs (16-byte aligned base):
  * D = rowsum(G_O * O) [B,H,n] fp32, the fp32 dQ accumulator [B,n,H,d], a
  * device status word and the backward kernel's work-item counter.  The call

@@ -313,3 +313,18 @@ def test_varlen_splits_runs_longer_than_the_grid_limit(lib):
     # one D area (256-byte rounded) and one dQ area per group, one 16-byte slot each
     want = sum(-(-(b * 2 * 4) // 256) * 256 + b * 2 * 64 * 4 for b in (65535, 4465)) + 2 * 16
     assert sz.bwd_workspace_bytes == want
+
+
+def test_list_sizes_match_the_documented_layout(lib):
+    from block_sparse_attention_fwd_gb300 import _lib
+    s = _shape(B=2, n=1000, H=4, Hk=2, d=64, block_q=128, block_k=64)   # T_r 8, T_c 16
+    m, kv, kc, qi, qc, total = _lib.lists_elems(s)
+    assert (m, kv, kc, qi, qc) == (2 * 4 * 8 * 16, 2 * 4 * 8 * 16, 2 * 4 * 8, 2 * 4 * 16 * 8,
+                                   2 * 4 * 16)
+    assert total == m + 4 * (kv + kc + qi + qc)
+    got = _lib.alloc_lists(s, "cpu")                       # the binding allocates the same sizes
+    assert [got[k].numel() for k in ("mask", "kv_idx", "kv_cnt", "q_idx", "q_cnt")] == \
+        [m, kv, kc, qi, qc]
+    out = (ctypes.c_size_t * 5)()
+    assert lib.bl_lists_elems(ctypes.byref(_shape(d=96)), out) == 0
+    assert lib.bl_lists_elems(ctypes.byref(s), None) == 0
