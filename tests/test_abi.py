@@ -328,3 +328,32 @@ def test_list_sizes_match_the_documented_layout(lib):
     out = (ctypes.c_size_t * 5)()
     assert lib.bl_lists_elems(ctypes.byref(_shape(d=96)), out) == 0
     assert lib.bl_lists_elems(ctypes.byref(s), None) == 0
+
+
+def test_varlen_layout_matches_the_oracle_on_random_batches(lib):
+    """200 seeded random packings (empty sequences, runs of equal lengths,
+    both tile sizes): the library's sizes equal the oracle's layout and its
+    launch groups are the runs of equal non-zero lengths."""
+    import numpy as np
+    from block_sparse_attention_fwd_gb300 import _lib
+    from oracle import varlen as OV
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        nseq = int(rng.integers(1, 12))
+        pool = rng.integers(0, 700, size=3)
+        lens = [int(pool[rng.integers(0, 3)]) if rng.random() < 0.5 else int(rng.integers(0, 700))
+                for _ in range(nseq)]
+        if sum(lens) == 0:
+            lens[0] = 1
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(int).tolist()
+        bq, bk = (int(x) for x in rng.choice([64, 128], size=2))
+        causal = int(bq == 128 and bk == 128 and rng.random() < 0.5)
+        v, arr = _varlen(cu, H=2, Hk=1, d=64, block_q=bq, block_k=bk, causal=causal)
+        sz = _lib.VarlenSizes()
+        assert lib.bl_varlen_layout(ctypes.byref(v), ctypes.byref(sz)) == 0
+        _, tot = OV.layout(cu, 2, bq, bk)
+        assert (sz.total, sz.lse, sz.tile_stats, sz.mask, sz.kv_cnt, sz.q_idx, sz.q_cnt) == \
+            (tot["total"], tot["lse"], tot["stats"], tot["mask"], tot["kv_cnt"], tot["q_idx"],
+             tot["q_cnt"]), (cu, bq, bk)
+        nz = [n for n in lens if n]
+        assert sz.groups == sum(1 for i, n in enumerate(nz) if i == 0 or nz[i - 1] != n)
