@@ -343,6 +343,7 @@ def test_varlen_layout_matches_the_oracle_on_random_batches(lib):
         pool = rng.integers(0, 700, size=3)
         lens = [int(pool[rng.integers(0, 3)]) if rng.random() < 0.5 else int(rng.integers(0, 700))
                 for _ in range(nseq)]
+        lens = [0 if rng.random() < 0.15 else n for n in lens]      # empty sequences
         if sum(lens) == 0:
             lens[0] = 1
         cu = np.concatenate([[0], np.cumsum(lens)]).astype(int).tolist()
@@ -355,5 +356,6 @@ def test_varlen_layout_matches_the_oracle_on_random_batches(lib):
         assert (sz.total, sz.lse, sz.tile_stats, sz.mask, sz.kv_cnt, sz.q_idx, sz.q_cnt) == \
             (tot["total"], tot["lse"], tot["stats"], tot["mask"], tot["kv_cnt"], tot["q_idx"],
              tot["q_cnt"]), (cu, bq, bk)
-        nz = [n for n in lens if n]
-        assert sz.groups == sum(1 for i, n in enumerate(nz) if i == 0 or nz[i - 1] != n)
+        # a group is a run of consecutive sequences of one non-zero length (an
+        # empty sequence ends a run)
+        assert sz.groups == sum(1 for i, n in enumerate(lens) if n and (i == 0 or lens[i - 1] != n))
