@@ -1,15 +1,18 @@
 """Benchmark of the BackLite hot path on one GB300 (or N, one process each).
 
-One step = exact forward with tile statistics -> mask_from_stats -> block-
-sparse backward, on the video-DiT-shaped workload (B=1, H=Hk=40, n=32760 =
-21x30x52 latent grid, d=128, 128x128 tiles, negl_prob=0.05, clustered
-synthetic inputs, seed 0).  Inputs are resident in HBM and larger than the
-129 MB L2 (Q alone is 335 MB), so no flush is needed between steps.
+One step = exact forward that reduces the tile weights in its epilogue ->
+mask from the tile weights -> block-sparse backward, on the video-DiT-shaped
+workload (B=1, H=Hk=40, n=32760 = 21x30x52 latent grid, d=128, 128x128
+tiles, negl_prob=0.05, clustered synthetic inputs, seed 0).  Inputs are
+resident in HBM and larger than the 129 MB L2 (Q alone is 335 MB), so no
+flush is needed between steps.  The unfused path (forward writing the full
+statistics, bl_mask_from_stats reading them; the same lists) is timed beside
+it under "unfused".
 
 Printed JSON line (rank 0): ``value`` = attention-backward milliseconds per
-step (mask_from_stats + backward, CUDA events on the launch stream, max over
-ranks), with dense-equivalent TFLOP/s, skipped-tile fraction and the
-fraction of the measured bf16 tensor peak on the computed tiles beside it.
+step (mask + backward, CUDA events on the launch stream, max over ranks),
+with dense-equivalent TFLOP/s, skipped-tile fraction and the fraction of the
+measured bf16 tensor peak on the computed tiles beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -256,19 +259,23 @@ def run_ours(args):
     qd, kd, vd, god = (x.to(dev) for x in (q, k, v, go))
     o = torch.empty_like(qd)
     lse = torch.empty((w.B, w.H, w.n), dtype=torch.float32, device=dev)
-    stats = torch.empty((w.B, w.H, T_c, T_r * w.block_q), dtype=torch.float32, device=dev)
+    logw = torch.empty((w.B, w.H, T_r, T_c), dtype=torch.float32, device=dev)
+    fws = torch.empty(_lib.fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
     lists = _lib.alloc_lists(shape, dev)
     g_q, g_k, g_v = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # one step: the forward reduces the tile weights in its epilogue (the
+    # statistics rows stay in its scratch slots), the mask reads the weights,
+    # then the block-sparse backward
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        _lib.attn_fwd(shape, qd, kd, vd, w.scale, o, lse, stats)
+        _lib.attn_fwd_tile_weights(shape, qd, kd, vd, w.scale, o, lse, logw, workspace=fws)
         if ev:
             ev[1].record(stream)
-        _lib.mask_from_stats(shape, stats, lse, negl, lists)
+        _lib.mask_from_tile_weights(shape, logw, negl, lists)
         if ev:
             ev[2].record(stream)
         _lib.attn_bwd(shape, qd, kd, vd, o, god, lse, w.scale, lists, g_q, g_k, g_v, wsb)
@@ -322,7 +329,27 @@ def run_ours(args):
         b.record(stream)
         torch.cuda.synchronize()
         dense_ms.append(a.elapsed_time(b))
-    # restore the sparse gradients (not needed for timing; keeps buffers meaningful)
+    # the unfused path beside it: the forward writing the full statistics and
+    # the mask pass reading them (the same lists, bit for bit)
+    def timed_call(fn, reps=3):
+        ts = []
+        for _ in range(reps + 1):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts[1:])
+
+    stats = torch.empty((w.B, w.H, T_c, T_r * w.block_q), dtype=torch.float32, device=dev)
+    fwd_stats_ms = timed_call(lambda: _lib.attn_fwd(shape, qd, kd, vd, w.scale, o, lse, stats))
+    lists2 = _lib.alloc_lists(shape, dev)
+    mask_stats_ms = timed_call(lambda: _lib.mask_from_stats(shape, stats, lse, negl, lists2))
+    if not torch.equal(lists2["mask"], lists["mask"]):
+        raise RuntimeError("the mask from the tile weights differs from the mask from the stats")
+    del stats, lists2
 
     pk = _peaks()
     dense_flop = w.dense_bwd_flop()
@@ -364,11 +391,16 @@ def run_ours(args):
                                    "valid keys per kept tile; traffic summed over the three",
                          "peak_src": pk["src"] + " burst"},
         "roofline_mask": {"bound": "hbm",
-                          "achieved": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
+                          "achieved": _mask_bytes(w, True) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
                           "peak": pk["hbm"], "unit": "GB/s",
-                          "frac": _mask_bytes(w) / (statistics.mean(mask_ms) * 1e-3) / 1e9 / pk["hbm"],
-                          "traffic": _sum_or_none(traffic, ("mask_rows_kernel", "q_lists_kernel")),
-                          "kernel": "bl_mask_from_stats call (mask_rows_kernel + q_lists_kernel)"},
+                          "frac": _mask_bytes(w, True) / (statistics.mean(mask_ms) * 1e-3) / 1e9 / pk["hbm"],
+                          "traffic": None,
+                          "kernel": "bl_mask_from_tile_weights call (mask_rows_kernel + "
+                                    "q_lists_kernel) reading the forward's tile weights"},
+        "unfused": {"fwd_with_stats_ms": fwd_stats_ms, "mask_from_stats_ms": mask_stats_ms,
+                    "mask_from_stats_gbs": _mask_bytes(w) / (mask_stats_ms * 1e-3) / 1e9,
+                    "what": "forward writing the full tile statistics + bl_mask_from_stats "
+                            "(same lists); not part of value"},
         # per step: forward 1, mask 2, backward 3 (D pass, tcgen05 pass, dQ convert)
         "gpu_launches": 6 * args.steps,
     }
@@ -389,13 +421,16 @@ def run_ours(args):
     return 0
 
 
-def _mask_bytes(w):
-    """Algorithmic bytes of bl_mask_from_stats: read the tile statistics and
-    the LSE, write mask, kv_idx, kv_cnt, q_idx, q_cnt."""
-    stats = w.B * w.H * w.T_c * w.T_r * w.block_q * 4
-    lse = w.B * w.H * w.n * 4
+def _mask_bytes(w, from_weights=False):
+    """Algorithmic bytes of the mask pass: read the tile statistics and the
+    LSE (bl_mask_from_stats) or the tile weights (bl_mask_from_tile_weights),
+    write mask, kv_idx, kv_cnt, q_idx, q_cnt."""
+    if from_weights:
+        inp = w.B * w.H * w.T_r * w.T_c * 4
+    else:
+        inp = w.B * w.H * w.T_c * w.T_r * w.block_q * 4 + w.B * w.H * w.n * 4
     lists = w.B * w.H * w.T_r * w.T_c * (1 + 4 + 4) + w.B * w.H * (w.T_r + w.T_c) * 4
-    return stats + lse + lists
+    return inp + lists
 
 
 def _sum_or_none(traffic, kernels):
@@ -448,7 +483,8 @@ def _e2e(args, w, shape, q, k, v, go, negl, dev):
     o = torch.empty_like(dq)
     lse = torch.empty((w.B, w.H, w.n), dtype=torch.float32, device=dev)
     T_r, T_c = _lib.tiles(shape)
-    stats = torch.empty((w.B, w.H, T_c, T_r * w.block_q), dtype=torch.float32, device=dev)
+    logw = torch.empty((w.B, w.H, T_r, T_c), dtype=torch.float32, device=dev)
+    fws = torch.empty(_lib.fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
     lists = _lib.alloc_lists(shape, dev)
     gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
     wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
@@ -463,8 +499,8 @@ def _e2e(args, w, shape, q, k, v, go, negl, dev):
             go_ready.record(copy)
         for dst, src in ((dq, hq), (dk, hk), (dv, hv)):
             dst.copy_(src, non_blocking=True)
-        _lib.attn_fwd(shape, dq, dk, dv, w.scale, o, lse, stats)
-        _lib.mask_from_stats(shape, stats, lse, negl, lists)
+        _lib.attn_fwd_tile_weights(shape, dq, dk, dv, w.scale, o, lse, logw, workspace=fws)
+        _lib.mask_from_tile_weights(shape, logw, negl, lists)
         stream.wait_event(go_ready)
         _lib.attn_bwd(shape, dq, dk, dv, o, dg, lse, w.scale, lists, gq, gk, gv, wsb)
         for dst, src in zip(outs, (gq, gk, gv)):

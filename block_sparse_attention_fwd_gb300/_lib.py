@@ -20,8 +20,9 @@ BL_STATUS = {0: "BL_OK", 1: "BL_ERR_INVALID_ARG", 2: "BL_ERR_UNSUPPORTED", 3: "B
 
 # Every symbol include/bl_attn.h declares (checked by the CPU test suite).
 EXPORTS = ("bl_tile_stats_elems", "bl_lists_elems", "bl_bwd_workspace_bytes", "bl_attn_fwd",
-           "bl_mask_from_stats", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
-           "bl_attn_bwd_noalloc", "bl_lse_combine", "bl_grad_error", "bl_varlen_layout",
+           "bl_mask_from_stats", "bl_fwd_workspace_bytes", "bl_attn_fwd_tile_weights",
+           "bl_mask_from_tile_weights", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
+           "bl_attn_bwd_noalloc", "bl_bwd_noalloc_check_status", "bl_lse_combine", "bl_grad_error", "bl_varlen_layout",
            "bl_attn_fwd_varlen", "bl_mask_from_stats_varlen", "bl_attn_bwd_varlen",
            "bl_varlen_bwd_check_status")
 
@@ -83,10 +84,18 @@ def load():
     lib.bl_attn_fwd.restype = ctypes.c_int
     lib.bl_mask_from_stats.argtypes = [S, P, P, D, ctypes.POINTER(Lists), P]
     lib.bl_mask_from_stats.restype = ctypes.c_int
+    lib.bl_fwd_workspace_bytes.argtypes = [S]
+    lib.bl_fwd_workspace_bytes.restype = Z
+    lib.bl_attn_fwd_tile_weights.argtypes = [S, P, P, P, F, P, P, P, P, P, Z, P]
+    lib.bl_attn_fwd_tile_weights.restype = ctypes.c_int
+    lib.bl_mask_from_tile_weights.argtypes = [S, P, D, ctypes.POINTER(Lists), P]
+    lib.bl_mask_from_tile_weights.restype = ctypes.c_int
     lib.bl_attn_bwd.argtypes = [S, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P, P, Z, P]
     lib.bl_attn_bwd.restype = ctypes.c_int
     lib.bl_attn_bwd_noalloc.argtypes = [S, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P, P]
     lib.bl_attn_bwd_noalloc.restype = ctypes.c_int
+    lib.bl_bwd_noalloc_check_status.argtypes = [S, P]
+    lib.bl_bwd_noalloc_check_status.restype = ctypes.c_int
     lib.bl_lse_combine.argtypes = [ctypes.c_int] * 5 + [P, P, P, P, P]
     lib.bl_lse_combine.restype = ctypes.c_int
     lib.bl_grad_error.argtypes = [P, P, Z, P, P]
@@ -175,6 +184,54 @@ def attn_fwd(shape, q, k, v, scale, o, lse, tile_stats=None):
     _check("bl_attn_fwd", code)
 
 
+def fwd_workspace_bytes(shape: Shape) -> int:
+    """Scratch of attn_fwd_tile_weights without a statistics output (current device)."""
+    return int(load().bl_fwd_workspace_bytes(ctypes.byref(shape)))
+
+
+def attn_fwd_tile_weights(shape, q, k, v, scale, o, lse, tile_logw, tile_stats=None,
+                          workspace=None):
+    """bl_attn_fwd_tile_weights: the forward that also reduces the tile weights
+    tile_logw [B,H,T_r,T_c] fp32; without tile_stats the statistics rows live
+    only in `workspace` (uint8, at least fwd_workspace_bytes)."""
+    B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
+    T_r, T_c = tiles(shape)
+    _need(q, torch.bfloat16, (B, n, H, d), "q")
+    _need(k, torch.bfloat16, (B, n, Hk, d), "k")
+    _need(v, torch.bfloat16, (B, n, Hk, d), "v")
+    _need(o, torch.bfloat16, (B, n, H, d), "o")
+    _need(lse, torch.float32, (B, H, n), "lse")
+    _need(tile_logw, torch.float32, (B, H, T_r, T_c), "tile_logw")
+    if tile_stats is not None:
+        _need(tile_stats, torch.float32, (B, H, T_c, T_r * shape.block_q), "tile_stats")
+    nbytes = 0
+    if workspace is not None:
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+            raise TypeError("workspace must be a CUDA uint8 tensor")
+        nbytes = workspace.numel()
+    code = load().bl_attn_fwd_tile_weights(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                           float(scale), _ptr(o), _ptr(lse), _ptr(tile_stats),
+                                           _ptr(tile_logw), _ptr(workspace), nbytes,
+                                           _stream(q.device))
+    _check("bl_attn_fwd_tile_weights", code)
+
+
+def mask_from_tile_weights(shape, tile_logw, negl_prob, lists):
+    B, H = shape.B, shape.H
+    T_r, T_c = tiles(shape)
+    _need(tile_logw, torch.float32, (B, H, T_r, T_c), "tile_logw")
+    _need(lists["mask"], torch.uint8, (B, H, T_r, T_c), "mask")
+    _need(lists["kv_idx"], torch.int32, (B, H, T_r, T_c), "kv_idx")
+    _need(lists["kv_cnt"], torch.int32, (B, H, T_r), "kv_cnt")
+    _need(lists["q_idx"], torch.int32, (B, H, T_c, T_r), "q_idx")
+    _need(lists["q_cnt"], torch.int32, (B, H, T_c), "q_cnt")
+    ls = _lists_struct(lists)
+    code = load().bl_mask_from_tile_weights(ctypes.byref(shape), _ptr(tile_logw),
+                                            float(negl_prob), ctypes.byref(ls),
+                                            _stream(tile_logw.device))
+    _check("bl_mask_from_tile_weights", code)
+
+
 def alloc_lists(shape: Shape, device) -> dict:
     T_r, T_c = tiles(shape)
     B, H = shape.B, shape.H
@@ -254,6 +311,12 @@ def attn_bwd_noalloc(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v):
                                       ctypes.byref(ls) if ls is not None else None,
                                       _ptr(g_q), _ptr(g_k), _ptr(g_v), _stream(q.device))
     _check("bl_attn_bwd_noalloc", code)
+
+
+def bwd_noalloc_check_status(shape, device=None) -> int:
+    """bl_bwd_noalloc_check_status: the status word of the last no-alloc backward."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return int(load().bl_bwd_noalloc_check_status(ctypes.byref(shape), _stream(dev)))
 
 
 def lse_combine(o_parts, lse_parts, o, lse):

@@ -95,9 +95,55 @@ bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats, con
   if (!aligned16(tile_stats) || !aligned16(lse)) return BL_ERR_INVALID_ARG;
   if (!(negl_prob >= 0.0) || !(negl_prob < 1.0)) return BL_ERR_INVALID_ARG;
   if (sh.T_c > 2048) return BL_ERR_UNSUPPORTED;
-  return cuda_status(bl::launch_mask(sh, tile_stats, lse, bl::mask_threshold(negl_prob),
+  return cuda_status(bl::launch_mask(sh, tile_stats, lse, nullptr, bl::mask_threshold(negl_prob),
                                      lists->mask, lists->kv_idx, lists->kv_cnt, lists->q_idx,
                                      lists->q_cnt, lists->nan_count, (cudaStream_t)stream));
+}
+
+size_t bl_fwd_workspace_bytes(const bl_shape* shape) {
+  bl::Shape sh;
+  if (check_shape(shape, &sh) != BL_OK || !bl::fwd_tc_supported(sh) || sh.T_c > 2048) return 0;
+  return bl::fwd_scratch_bytes(sh);
+}
+
+bl_status bl_attn_fwd_tile_weights(const bl_shape* shape, const void* q, const void* k,
+                                   const void* v, float scale, void* o, float* lse,
+                                   float* tile_stats, float* tile_logw, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  bl::Shape sh;
+  bl_status s = check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  if (!q || !k || !v || !o || !lse || !tile_logw) return BL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(tile_logw) || (tile_stats && !aligned16(tile_stats)))
+    return BL_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
+  if (!bl::fwd_tc_supported(sh) || sh.T_c > 2048) return BL_ERR_UNSUPPORTED;
+  if (!tile_stats) {
+    const size_t need = bl::fwd_scratch_bytes(sh);
+    if (need == 0) return BL_ERR_CUDA;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return BL_ERR_WORKSPACE;
+  }
+  return cuda_status(bl::launch_fwd_tc(sh, q, k, v, o, lse, tile_stats, tile_logw,
+                                       tile_stats ? nullptr : workspace, scale,
+                                       (cudaStream_t)stream));
+}
+
+bl_status bl_mask_from_tile_weights(const bl_shape* shape, const float* tile_logw,
+                                    double negl_prob, const bl_lists* lists, void* stream) {
+  bl::Shape sh;
+  bl_status s = check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  if (!tile_logw || !lists) return BL_ERR_INVALID_ARG;
+  if (!lists->mask || !lists->kv_idx || !lists->kv_cnt || !lists->q_idx || !lists->q_cnt)
+    return BL_ERR_INVALID_ARG;
+  if (!aligned16(tile_logw)) return BL_ERR_INVALID_ARG;
+  if (!(negl_prob >= 0.0) || !(negl_prob < 1.0)) return BL_ERR_INVALID_ARG;
+  if (sh.T_c > 2048) return BL_ERR_UNSUPPORTED;
+  return cuda_status(bl::launch_mask(sh, nullptr, nullptr, tile_logw,
+                                     bl::mask_threshold(negl_prob), lists->mask, lists->kv_idx,
+                                     lists->kv_cnt, lists->q_idx, lists->q_cnt, lists->nan_count,
+                                     (cudaStream_t)stream));
 }
 
 bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k, const void* v,

@@ -76,3 +76,24 @@ extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, c
                                  ws_status, (cudaStream_t)stream);
   return e == cudaSuccess ? BL_OK : BL_ERR_CUDA;
 }
+
+// The status word of the last bl_attn_bwd_noalloc call on this device with
+// this shape: it sits in the scratch array where the workspace layout of that
+// shape puts it.  Reading it allocates nothing either.
+extern "C" bl_status bl_bwd_noalloc_check_status(const bl_shape* shape, void* stream) {
+  bl::Shape sh;
+  bl_status s = bl::check_shape(shape, &sh);
+  if (s != BL_OK) return s;
+  if (bl_bwd_workspace_bytes(shape) > (size_t)BL_NOALLOC_SCRATCH_BYTES) return BL_ERR_WORKSPACE;
+  const unsigned char* ws = static_cast<const unsigned char*>(scratch_address());
+  if (!ws) return BL_ERR_CUDA;
+  const int32_t* st =
+      reinterpret_cast<const int32_t*>(ws + bl::ws_D_bytes(sh) + bl::ws_dq_bytes(sh));
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, st, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                  (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return BL_ERR_CUDA;
+  if (host & 2) return BL_ERR_TIMEOUT;
+  return (host & 1) ? BL_ERR_CORRUPT_LISTS : BL_OK;
+}

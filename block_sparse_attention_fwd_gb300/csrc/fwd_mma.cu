@@ -209,7 +209,8 @@ cudaError_t launch_fwd_t(const Shape& sh, const void* q, const void* k, const vo
 
 cudaError_t launch_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                        float* lse, float* stats, float scale, cudaStream_t st) {
-  if (fwd_tc_supported(sh)) return launch_fwd_tc(sh, q, k, v, o, lse, stats, nullptr, scale, st);
+  if (fwd_tc_supported(sh))
+    return launch_fwd_tc(sh, q, k, v, o, lse, stats, nullptr, nullptr, scale, st);
   if (sh.d == 64 && sh.block_k == 64) return launch_fwd_t<64, 64>(sh, q, k, v, o, lse, stats, scale, st);
   if (sh.d == 64 && sh.block_k == 128) return launch_fwd_t<64, 128>(sh, q, k, v, o, lse, stats, scale, st);
   if (sh.d == 128 && sh.block_k == 64) return launch_fwd_t<128, 64>(sh, q, k, v, o, lse, stats, scale, st);

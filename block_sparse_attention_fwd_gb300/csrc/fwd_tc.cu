@@ -67,11 +67,29 @@ struct FBars {
 
 __device__ __forceinline__ bool failed(const int* f) { return *(volatile const int*)f != 0; }
 
+// max that propagates NaN (one operation carries the maximum and the "some
+// term is NaN" flag of a reduction)
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Scratch for the tile weights without a statistics output: `nslots` slots
+// of [T_c][256] floats (the two query tiles' rows of every key tile), one per
+// CTA that can be resident at once, each claimed with a lock word.
+struct RowScratch {
+  float* slots;
+  int32_t* locks;
+  int nslots;
+};
+
 template <int D>
 __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
-    float* __restrict__ lse, float* __restrict__ stats, Shape sh, float scale_log2) {
+    float* __restrict__ lse, float* __restrict__ stats, float* __restrict__ logw,
+    RowScratch scr, Shape sh, float scale_log2) {
   using C = FCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -79,6 +97,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   __shared__ __align__(8) FBars bars;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
+  __shared__ int s_slot;
+  __shared__ float s_lse[256];   // the pair's final LSE rows (tile weights)
+  __shared__ __align__(8) uint64_t s_wbar[2];   // statistics staging buffers (tile weights)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // under causal structure later pairs visit more key tiles: start them first
@@ -108,7 +129,27 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       mbar_init(&bars.p_ready[t], 128);
       mbar_init(&bars.o_done[t], 1);
     }
+    mbar_init(&s_wbar[0], 1);
+    mbar_init(&s_wbar[1], 1);
     s_fail = 0;
+    // without a statistics output the rows go to a scratch slot of this CTA's
+    // own (claimed from a lock word; at most nslots CTAs are resident at once)
+    s_slot = -1;
+    if (!stats && logw && scr.slots) {
+      // start at this SM's own slot: the CTA that ran here before released it
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      const uint64_t t0 = globaltimer();
+      for (int tries = 0;; ++tries) {
+        const int sl = (int)((smid + tries) % scr.nslots);
+        if (atomicCAS(&scr.locks[sl], 0, 1) == 0) {
+          __threadfence();
+          s_slot = sl;
+          break;
+        }
+        if (tries % scr.nslots == scr.nslots - 1 && globaltimer() - t0 > kWaitLimitNs) break;
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&s_tmem, C::T_COLS);
@@ -222,7 +263,17 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     const uint32_t o_col = lane_base + C::T_O + t * D;
     const int64_t bh = (int64_t)b * sh.H + h;
     const bool valid_tile = t < ntile;
-    float* st_row = stats ? stats + bh * sh.T_c * sh.n_pad + row : nullptr;
+    // this row's statistic of key tile j lives at st_row[j * st_stride]: in the
+    // statistics output, else in the CTA's scratch slot (tile weights only)
+    float* st_row = nullptr;
+    int st_stride = 0;
+    if (stats) {
+      st_row = stats + bh * sh.T_c * sh.n_pad + row;
+      st_stride = (int)sh.n_pad;
+    } else if (s_slot >= 0) {
+      st_row = scr.slots + (int64_t)s_slot * sh.T_c * 256 + t * 128 + r;
+      st_stride = 256;
+    }
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = valid_tile;
     for (int jj = 0; ok && jj < nj; ++jj) {
@@ -268,7 +319,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       for (int c = 0; c < 4; ++c)
         tmem_st16(s_col + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&x[c * 16]));
       if (st_row)
-        st_row[(int64_t)j * sh.n_pad] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
+        st_row[(int64_t)j * st_stride] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
       l_run = l_run * alpha + ts;
       m_ref = m_new;
       // rescale O in TMEM (rare).  S_t(jj) has completed, hence so has
@@ -292,7 +343,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     if (valid_tile) {
       if (!ok && lane == 0) fail();
       // key tiles this pair never visits carry no weight for this row
-      if (st_row) {
+      if (stats) {
         for (int j = 0; j < j_lo; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
         for (int j = j_hi + 1; j < Tc; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
       }
@@ -321,21 +372,100 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
         }
       }
       // a forward that gave up on a bounded wait marks its rows' LSE with NaN
-      if (row < sh.n)
-        lse[bh * sh.n + row] =
-            done ? (m_ref + __log2f(l_run)) * kLn2 : __uint_as_float(0x7fc00000u);
+      const float lse_v = done ? (m_ref + __log2f(l_run)) * kLn2 : __uint_as_float(0x7fc00000u);
+      if (row < sh.n) lse[bh * sh.n + row] = lse_v;
       if (!done && lane == 0) fail();
+      if (logw) s_lse[t * 128 + r] = lse_v;
+    }
+    if (logw) {
+      // Tile weights of the pair's query tiles: d_ij = max over the tile's
+      // rows r < n of fp32(LSE_{r,j} - LSE_r) (NaN if any term is NaN),
+      // clamped to <= 0 with -0 -> +0; key tiles outside tile i's attending
+      // range enter with LSE_{r,j} = -inf.  Every MMA has completed, so the
+      // dynamic shared memory is free: the pair's statistics rows (1 KB per
+      // key tile: 128 rows of each query tile) come in with bulk copies, in
+      // chunks of JB key tiles into two alternating buffers, while the eight
+      // softmax warps reduce the previous chunk, one warp per (query tile,
+      // key tile): a float4 of rows per lane, then shuffles.
+      fence_proxy_async_global();   // this thread's statistics, for the copies
+      named_sync(1, 256);
+      const int ww = warp - 4;                       // 0..7
+      constexpr int JB = C::BYTES / 2 / 1024;        // key tiles per buffer
+      const int nchunks = (Tc + JB - 1) / JB;
+      int lo0, hi0, lo1 = 0, hi1 = -1;
+      key_tile_range(sh, 2 * pair, lo0, hi0);
+      if (ntile == 2) key_tile_range(sh, 2 * pair + 1, lo1, hi1);
+      // row block of key tile j: gsrc + j * gstride floats
+      const float* gsrc = stats ? stats + bh * sh.T_c * sh.n_pad + pair * 256
+                                : (s_slot >= 0 ? scr.slots + (int64_t)s_slot * Tc * 256 : nullptr);
+      const int64_t gstride = stats ? sh.n_pad : 256;
+      const uint32_t rowbytes = (stats && ntile == 1) ? 512u : 1024u;
+      const bool issuer = ww == 0 && lane == 0 && gsrc != nullptr;
+      auto issue = [&](int c) {
+        const int j0 = c * JB, jn = min(JB, Tc - j0);
+        uint8_t* dst = sm + (c & 1) * JB * 1024;
+        mbar_expect_tx(&s_wbar[c & 1], (uint32_t)jn * rowbytes);
+        if (!stats) {
+          bulk_load(dst, gsrc + (int64_t)j0 * 256, (uint32_t)jn * 1024u, &s_wbar[c & 1]);
+        } else {
+          for (int jj = 0; jj < jn; ++jj)
+            bulk_load(dst + jj * 1024, gsrc + (int64_t)(j0 + jj) * gstride, rowbytes,
+                      &s_wbar[c & 1]);
+        }
+      };
+      if (issuer) {
+        issue(0);
+        if (nchunks > 1) issue(1);
+      }
+      for (int c = 0; c < nchunks; ++c) {
+        const int j0 = c * JB, jn = min(JB, Tc - j0);
+        const bool have = gsrc != nullptr && mbar_wait(&s_wbar[c & 1], (c >> 1) & 1);
+        const float* buf = reinterpret_cast<const float*>(sm + (c & 1) * JB * 1024);
+        for (int tt = 0; tt < ntile; ++tt) {
+          const int lo = tt ? lo1 : lo0, hi = tt ? hi1 : hi0;
+          const int r0 = (2 * pair + tt) * 128 + 4 * lane;
+          const float* l4 = s_lse + tt * 128 + 4 * lane;
+          float* wrow = logw + (bh * sh.T_r + 2 * pair + tt) * (int64_t)Tc;
+          for (int jj = ww; jj < jn; jj += 8) {
+            const int j = j0 + jj;
+            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (j >= lo && j <= hi)
+              v = have ? reinterpret_cast<const float4*>(buf + jj * 256 + tt * 128)[lane]
+                       : make_float4(__uint_as_float(0x7fc00000u), 0.f, 0.f, 0.f);
+            float mx = -INFINITY;
+            if (r0 < sh.n) mx = max_nan(mx, __fsub_rn(v.x, l4[0]));
+            if (r0 + 1 < sh.n) mx = max_nan(mx, __fsub_rn(v.y, l4[1]));
+            if (r0 + 2 < sh.n) mx = max_nan(mx, __fsub_rn(v.z, l4[2]));
+            if (r0 + 3 < sh.n) mx = max_nan(mx, __fsub_rn(v.w, l4[3]));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+              mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane == 0) {
+              float dv = isnan(mx) ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
+              if (dv == 0.f) dv = 0.f;   // -0 -> +0
+              wrow[j] = dv;
+            }
+          }
+        }
+        named_sync(1, 256);          // every warp is done with this buffer
+        if (issuer && c + 2 < nchunks) issue(c + 2);
+      }
     }
   }
 
   fence_before_sync();
   __syncthreads();
   if (warp == 1) tmem_free(tmem, C::T_COLS);
+  if (threadIdx.x == 0 && s_slot >= 0) {   // the slot's rows have all been read
+    __threadfence();
+    atomicExch(&scr.locks[s_slot], 0);
+  }
 }
 
 template <int D>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, void* o,
-                     float* lse, float* stats, float scale, cudaStream_t st) {
+                     float* lse, float* stats, float* logw, RowScratch scr, float scale,
+                     cudaStream_t st) {
   using C = FCfg<D>;
   CUtensorMap mq, mk, mv;
   if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
@@ -346,9 +476,31 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   auto kern = fwd_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (scr.locks) {
+    e = cudaMemsetAsync(scr.locks, 0, (size_t)scr.nslots * sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid((sh.T_r + 1) / 2, sh.H, sh.B);
-  kern<<<grid, 384, smem, st>>>(mq, mk, mv, (__nv_bfloat16*)o, lse, stats, sh, scale * kLog2e);
+  kern<<<grid, 384, smem, st>>>(mq, mk, mv, (__nv_bfloat16*)o, lse, stats, logw, scr, sh,
+                                scale * kLog2e);
   return cudaGetLastError();
+}
+
+// CTAs of the forward that can be resident on the current device at once.
+template <int D>
+int resident_ctas() {
+  using C = FCfg<D>;
+  const int smem = C::BYTES + 1024;
+  auto kern = fwd_tc_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return 0;
+  int occ = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 384, smem) != cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return occ * sms;
 }
 
 }  // namespace
@@ -357,12 +509,27 @@ bool fwd_tc_supported(const Shape& sh) {
   return sh.block_q == 128 && sh.block_k == 128 && (sh.d == 64 || sh.d == 128);
 }
 
+size_t fwd_scratch_bytes(const Shape& sh) {
+  const int ns = sh.d == 128 ? resident_ctas<128>() : resident_ctas<64>();
+  if (ns <= 0) return 0;
+  const size_t locks = ((size_t)ns * sizeof(int32_t) + 255) & ~(size_t)255;
+  return locks + (size_t)ns * sh.T_c * 256 * sizeof(float);
+}
+
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
-                          float* lse, float* stats, int32_t* status, float scale,
+                          float* lse, float* stats, float* logw, void* scratch, float scale,
                           cudaStream_t st) {
-  (void)status;
-  if (sh.d == 128) return launch_t<128>(sh, q, k, v, o, lse, stats, scale, st);
-  return launch_t<64>(sh, q, k, v, o, lse, stats, scale, st);
+  RowScratch scr{nullptr, nullptr, 0};
+  if (logw && !stats) {
+    const int ns = sh.d == 128 ? resident_ctas<128>() : resident_ctas<64>();
+    if (ns <= 0 || !scratch) return cudaErrorInvalidValue;
+    const size_t locks = ((size_t)ns * sizeof(int32_t) + 255) & ~(size_t)255;
+    scr.locks = static_cast<int32_t*>(scratch);
+    scr.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + locks);
+    scr.nslots = ns;
+  }
+  if (sh.d == 128) return launch_t<128>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+  return launch_t<64>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
 }
 
 }  // namespace bl

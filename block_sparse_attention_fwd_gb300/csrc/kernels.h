@@ -14,11 +14,12 @@ cudaError_t launch_fwd(const Shape& sh, const void* q, const void* k, const void
                        float* lse, float* stats, float scale, cudaStream_t st);
 
 // Tile selection: per-query-tile mask row, kv list and count, then the
-// transposed per-key-tile q list and count.
+// transposed per-key-tile q list and count.  From the statistics and the
+// LSE, or (stats == nullptr) from the tile weights logw [B,H,T_r,T_c].
 cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
-                        unsigned long long threshold, uint8_t* mask, int32_t* kv_idx,
-                        int32_t* kv_cnt, int32_t* q_idx, int32_t* q_cnt, int32_t* nan_count,
-                        cudaStream_t st);
+                        const float* logw, unsigned long long threshold, uint8_t* mask,
+                        int32_t* kv_idx, int32_t* kv_cnt, int32_t* q_idx, int32_t* q_cnt,
+                        int32_t* nan_count, cudaStream_t st);
 
 // Backward.  q_idx/q_cnt == nullptr runs every tile.  ws_D [B,H,n] fp32,
 // ws_dq [B,n,H,d] fp32, ws_status one int32.
@@ -35,10 +36,13 @@ cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const v
                           const int32_t* q_idx, const int32_t* q_cnt, void* g_k, void* g_v,
                           float* dq_acc, int32_t* status, float scale, cudaStream_t st);
 
-// tcgen05 forward with tile statistics for 128 x 128 tiles (head dim 64 or 128).
+// tcgen05 forward with tile statistics for 128 x 128 tiles (head dim 64 or
+// 128).  logw != nullptr also writes the tile weights [B,H,T_r,T_c]; with
+// stats == nullptr their rows go through `scratch` (fwd_scratch_bytes).
 bool fwd_tc_supported(const Shape& sh);
+size_t fwd_scratch_bytes(const Shape& sh);
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
-                          float* lse, float* stats, int32_t* status, float scale,
+                          float* lse, float* stats, float* logw, void* scratch, float scale,
                           cudaStream_t st);
 
 // LSE-combine of `parts` partial results (layouts in include/bl_attn.h).

@@ -81,11 +81,14 @@ __device__ __forceinline__ uint32_t order_key(float d) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int RPL, int CAP>  // rows per lane: block_q / 32; capacity >= T_c
+// FROM_W: d_ij comes ready-made from the tile weights logw [B,H,T_r,T_c] that
+// the forward reduced (the same arithmetic as the reduction below).
+template <int RPL, int CAP, bool FROM_W>  // rows per lane: block_q / 32; capacity >= T_c
 __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
-    const float* __restrict__ stats, const float* __restrict__ lse, Shape sh,
-    unsigned long long T, uint8_t* __restrict__ mask, int32_t* __restrict__ kv_idx,
-    int32_t* __restrict__ kv_cnt, int32_t* __restrict__ nan_count) {
+    const float* __restrict__ stats, const float* __restrict__ lse,
+    const float* __restrict__ logw, Shape sh, unsigned long long T, uint8_t* __restrict__ mask,
+    int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
+    int32_t* __restrict__ nan_count) {
   __shared__ float s_d[CAP];
   __shared__ unsigned long long s_key[CAP];
   __shared__ unsigned long long s_E[CAP];
@@ -99,7 +102,10 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
   const int64_t bh = (int64_t)b * sh.H + h;
   int k_lo, k_hi;
   key_tile_range(sh, i, k_lo, k_hi);
-  {
+  if constexpr (FROM_W) {
+    const float* wrow = logw + (bh * sh.T_r + i) * (int64_t)Tc;
+    for (int j = tid; j < Tc; j += kMaskThreads) s_d[j] = wrow[j];
+  } else {
     const int r0 = i * sh.block_q + lane * RPL;
     float lrow[RPL];
     bool valid[RPL];
@@ -310,14 +316,20 @@ __global__ void __launch_bounds__(256) q_lists_kernel(const uint8_t* __restrict_
 }  // namespace
 
 cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
-                        unsigned long long threshold, uint8_t* mask, int32_t* kv_idx,
-                        int32_t* kv_cnt, int32_t* q_idx, int32_t* q_cnt, int32_t* nan_count,
-                        cudaStream_t st) {
+                        const float* logw, unsigned long long threshold, uint8_t* mask,
+                        int32_t* kv_idx, int32_t* kv_cnt, int32_t* q_idx, int32_t* q_cnt,
+                        int32_t* nan_count, cudaStream_t st) {
   if (sh.T_c > kMaxTc) return cudaErrorInvalidValue;
   dim3 g1(sh.T_r, sh.H, sh.B);
   auto rows = [&](auto rpl, auto cap) {
-    mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value>
-        <<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx, kv_cnt, nan_count);
+    if (stats)
+      mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value, false>
+          <<<g1, kMaskThreads, 0, st>>>(stats, lse, nullptr, sh, threshold, mask, kv_idx, kv_cnt,
+                                        nan_count);
+    else
+      mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value, true>
+          <<<g1, kMaskThreads, 0, st>>>(nullptr, nullptr, logw, sh, threshold, mask, kv_idx,
+                                        kv_cnt, nan_count);
   };
   auto by_cap = [&](auto rpl) {
     if (sh.T_c <= 256) rows(rpl, std::integral_constant<int, 256>{});

@@ -256,7 +256,8 @@ bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_s
   if (p.max_T_c > 2048) return BL_ERR_UNSUPPORTED;
   const unsigned long long T = bl::mask_threshold(negl_prob);
   return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
-    return bl::launch_mask(r.sh, tile_stats + r.stats, lse + r.lse, T, lists->mask + r.mask,
+    return bl::launch_mask(r.sh, tile_stats + r.stats, lse + r.lse, nullptr, T,
+                           lists->mask + r.mask,
                            lists->kv_idx + r.mask, lists->kv_cnt + r.kv_cnt,
                            lists->q_idx + r.q_idx, lists->q_cnt + r.q_cnt, lists->nan_count,
                            st);

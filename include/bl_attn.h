@@ -138,6 +138,56 @@ bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats,
                              const float* lse, double negl_prob,
                              const bl_lists* lists, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Tile weights reduced in the forward.
+ *
+ * The statistics hold n * T_c floats per head (17 GB at n = 131072 with 32
+ * heads), and the mask pass reads all of them.  The forward can instead
+ * reduce them itself, right after a query tile's last key tile, into the
+ * per-(query tile, key tile) log-weights the selection rule starts from
+ * ("BackLite" README, How It Works, Phase 2: p_tile = exp(LSE_tile - LSE_row);
+ * "Introducing BackLite", Training Nanochat, reports the stored statistics at
+ * about 1% of peak memory):
+ *   tile_logw : [B, H, T_r, T_c] fp32,
+ *               tile_logw[b,h,i,j] = d_ij = max over rows r < n of query tile
+ *               i of fp32(tile_stats[b,h,j,r] - lse[b,h,r]) (NaN if any term
+ *               is NaN), clamped to <= 0 with -0 stored as +0; key tiles that
+ *               no row of the tile attends (causal / window) enter with
+ *               tile_stats = -inf.  This is exactly the d_ij of
+ *               bl_mask_from_stats, bit for bit.
+ * 128 x 128 tiles (the tcgen05 forward) and T_c <= 2048 only.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of scratch bl_attn_fwd_tile_weights needs when tile_stats is NULL:
+ * one slot of 256 * T_c floats for every forward CTA that can be resident on
+ * the CURRENT device at once (about 152 * 256 * T_c * 4 bytes on a GB300),
+ * plus one lock word per slot.  0 for an invalid or unsupported shape. */
+size_t bl_fwd_workspace_bytes(const bl_shape* shape);
+
+/* bl_attn_fwd that also writes tile_logw (above).
+ *   tile_stats  the statistics output as in bl_attn_fwd, or NULL: then the
+ *               statistics rows live only in `workspace` (at least
+ *               bl_fwd_workspace_bytes, 16-byte aligned), one slot per
+ *               resident CTA, and are not returned.  Two calls in flight at
+ *               the same time must not share a workspace.  workspace may be
+ *               NULL when tile_stats is given.
+ * O, LSE and tile_stats are the same as bl_attn_fwd's, and tile_logw does not
+ * depend on whether tile_stats is given.
+ * Errors: as bl_attn_fwd; BL_ERR_UNSUPPORTED (tiles other than 128 x 128,
+ *         T_c > 2048); BL_ERR_WORKSPACE (tile_stats NULL and the workspace
+ *         missing or too small). */
+bl_status bl_attn_fwd_tile_weights(const bl_shape* shape, const void* q, const void* k,
+                                   const void* v, float scale, void* o, float* lse,
+                                   float* tile_stats, float* tile_logw, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* bl_mask_from_stats from the tile weights: the same lists, bit for bit, as
+ * bl_mask_from_stats on the statistics and LSE the weights were reduced from,
+ * reading T_r * T_c floats per head instead of n * T_c.
+ * Errors: as bl_mask_from_stats. */
+bl_status bl_mask_from_tile_weights(const bl_shape* shape, const float* tile_logw,
+                                    double negl_prob, const bl_lists* lists, void* stream);
+
 /* Masked attention backward ("Introducing BackLite", Backpropagation for
  * attention and Using Sparsity), with M the element mask expanded from
  * lists->mask and P recomputed from the full-row lse:
@@ -208,12 +258,21 @@ bl_status bl_grad_error(const void* a, const void* b, size_t n, double* out, voi
  * share the one array and it keeps the last call's contents (each call
  * clears what must start at zero), so calls that overlap on the GPU -- on
  * different streams, or from different threads -- race and must be
- * serialised by the caller.  The status word cannot be read back: list
- * entries out of range are skipped exactly as in bl_attn_bwd. */
+ * serialised by the caller.  List entries out of range are skipped exactly
+ * as in bl_attn_bwd and recorded in a status word inside the array, which
+ * bl_bwd_noalloc_check_status reads back. */
 bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, const void* k,
                               const void* v, const void* o, const void* g_o,
                               const float* lse, float scale, const bl_lists* lists,
                               void* g_q, void* g_k, void* g_v, void* stream);
+
+/* bl_bwd_check_status for bl_attn_bwd_noalloc: synchronises the stream and
+ * reads the status word the last bl_attn_bwd_noalloc call with this shape
+ * left in the fixed scratch array of the current device: BL_OK,
+ * BL_ERR_CORRUPT_LISTS, or BL_ERR_TIMEOUT (a bounded device-side wait gave
+ * up; that call's outputs are invalid).  Allocates nothing.  A later call
+ * with another shape moves the word, so read it before the next call. */
+bl_status bl_bwd_noalloc_check_status(const bl_shape* shape, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Packed variable-length batches.

@@ -106,17 +106,3 @@ def to_device_like(x_np, like):
     """An oracle array as a device tensor with the dtype/shape of ``like``."""
     return torch.from_numpy(np.ascontiguousarray(x_np)).to(dtype=like.dtype,
                                                             device=like.device)
-
-
-def chain_gq_tolerance(q, k, v, g_o, O, L, scale, mask, bq, bk, rows_sample=None):
-    """Tolerance for G_Q of a whole GPU chain (GPU O feeding the backward).
-
-    G_Q depends on O through D = rowsum(G_O * O), and G_P - D cancels on
-    peaked rows, so one-ulp differences in the bf16 O that any correct forward
-    may produce move G_Q.  The oracle measures that sensitivity itself: delta
-    = rel-L2 between G_Q formed from the exact O and from its bf16 rounding.
-    The chain is held to REL_L2 + 2 * delta."""
-    from oracle import attention as A
-    exact = A.backward(q, k, v, O, g_o, L, scale, mask, bq, bk)[0]
-    stored = A.backward(q, k, v, A.as_stored_output(O), g_o, L, scale, mask, bq, bk)[0]
-    return REL_L2 + 2.0 * rel_l2(stored, exact), stored

@@ -8,10 +8,11 @@ compute the masked gradients of the same mask.  The mask itself is checked
 bit for bit by applying the oracle's rule to the GPU's statistics.
 
 The long-context case (n = 131072) checks sampled query tiles against the
-oracle (forward rows, statistics, mask rows, G_Q) and the key-side gradients
-through a property that holds at any size: the gradients are linear in the
-mask, so the sparse gradients plus those of the complementary mask equal the
-dense gradients.
+oracle (forward rows, statistics, mask rows, G_Q), sampled key tiles of two
+whole GQA groups (G_K, G_V) element by element, and, at full size, a
+property that holds at any size: the gradients are linear in the mask, so
+the sparse gradients plus those of the complementary mask equal the dense
+gradients.
 """
 import numpy as np
 import pytest
@@ -145,7 +146,7 @@ def test_video_n32760_sampled_heads():
     q, k, v, go = inputs.generate(w, seed=0)
     shape, qd, kd, vd, o, lse, stats = _gpu_forward(w, q, k, v)
     lists = U.gpu_mask(shape, stats, lse, negl)
-    heads = [0, 27]
+    heads = [0, 13, 27, 39]
     orc, own = {}, {}
     for h in heads:
         orc[h] = _oracle_head(w, q, k, v, go, 0, h)
@@ -234,5 +235,33 @@ def test_long_n131072_sampled_rows_and_mask_linearity():
         s = a.float() + c.float()
         e = float((s - d.float()).norm() / d.float().norm())
         assert e <= U.REL_L2, e
-    del stats, lists, dev_lists, comp
+    del cq, ck, cv, dq, dk, dv, comp
+    # key-side gradients element by element against the oracle: sampled key
+    # tiles of two kv heads, each summed over its whole GQA group, from the
+    # same O, LSE and mask the GPU backward was given (its forward outputs,
+    # validated on the sampled rows above, with the oracle's rows injected)
+    G = w.H // w.Hk
+    key_tiles = (0, 333, 700, w.T_c - 1)
+    cols = np.concatenate([np.arange(j * 128, min(w.n, (j + 1) * 128)) for j in key_tiles])
+    for hk in (0, 5):
+        kh, vh = _head(k, 0, hk), _head(v, 0, hk)
+        rk = np.zeros((len(cols), w.d))
+        rv = np.zeros((len(cols), w.d))
+        for h in range(hk * G, (hk + 1) * G):
+            oh = o_in[0, :, h].float().cpu().double().numpy()
+            lh = lse_in[0, h].cpu().double().numpy()
+            _, bk, bv = A.backward_head(_head(q, 0, h), kh, vh, oh, _head(go, 0, h), lh, w.scale,
+                                        mask[0, h], 128, 128, cols=cols)
+            rk += bk
+            rv += bv
+        for t, j in enumerate(key_tiles):
+            sl = slice(t * 128, t * 128 + 128)
+            rows = cols[sl]
+            if np.linalg.norm(rv[sl]) == 0:           # no query tile kept this key tile
+                assert float(gk[0, rows, hk].abs().max()) == 0.0
+                assert float(gv[0, rows, hk].abs().max()) == 0.0
+                continue
+            assert U.rel_l2(U.cpu(gk[0, rows, hk]), rk[sl]) <= U.REL_L2, ("G_K", hk, j)
+            assert U.rel_l2(U.cpu(gv[0, rows, hk]), rv[sl]) <= U.REL_L2, ("G_V", hk, j)
+    del stats, lists, dev_lists
     _ = _lib
