@@ -76,8 +76,10 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 }
 
 // Scratch for the tile weights without a statistics output: `nslots` slots
-// of [T_c][256] floats (the two query tiles' rows of every key tile), one per
-// CTA that can be resident at once, each claimed with a lock word.
+// of [T_c][kRowStride] floats (the two query tiles' 256 rows of every key
+// tile, then 4 floats of padding), one per CTA that can be resident at once,
+// each claimed with a lock word.
+constexpr int kRowStride = 260;
 struct RowScratch {
   float* slots;
   int32_t* locks;
@@ -98,8 +100,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
   __shared__ int s_slot;
-  __shared__ float s_lse[256];   // the pair's final LSE rows (tile weights)
+  __shared__ __align__(16) float s_lse[256];   // the pair's final LSE rows (tile weights)
   __shared__ __align__(8) uint64_t s_wbar[2];   // statistics staging buffers (tile weights)
+  __shared__ int s_wissued;                      // the staging copies were requested
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // under causal structure later pairs visit more key tiles: start them first
@@ -271,8 +274,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       st_row = stats + bh * sh.T_c * sh.n_pad + row;
       st_stride = (int)sh.n_pad;
     } else if (s_slot >= 0) {
-      st_row = scr.slots + (int64_t)s_slot * sh.T_c * 256 + t * 128 + r;
-      st_stride = 256;
+      st_row = scr.slots + (int64_t)s_slot * sh.T_c * kRowStride + t * 128 + r;
+      st_stride = kRowStride;
     }
     float m_ref = -INFINITY, l_run = 0.f;
     bool ok = valid_tile;
@@ -347,6 +350,61 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
         for (int j = 0; j < j_lo; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
         for (int j = j_hi + 1; j < Tc; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
       }
+    }
+    // Tile weights of the pair's query tiles: d_ij = max over the tile's rows
+    // r < n of fp32(LSE_{r,j} - LSE_r) (NaN if any term is NaN), clamped to
+    // <= 0 with -0 -> +0; key tiles outside tile i's attending range enter
+    // with LSE_{r,j} = -inf.  Once every MMA has completed the dynamic shared
+    // memory is free: the pair's statistics rows (1 KB per key tile: 128 rows
+    // of each query tile) come in with bulk copies, in chunks of JB key tiles
+    // into two alternating buffers (rows of consecutive key tiles kRowStride
+    // floats apart).  The first two chunks are requested before the O rows
+    // are written out; the eight softmax warps then reduce chunk by chunk
+    // while the next one arrives.  One lane per key tile: a lane runs over the
+    // tile's rows with float4 loads (the 16-byte padding per key tile spreads
+    // the 32 lanes over all banks) and keeps its own maximum, so nothing
+    // waits on another lane.
+    const int ww = warp - 4;                         // 0..7
+    constexpr int JB = (C::BYTES / 2 / (kRowStride * 4)) / 32 * 32;   // key tiles per buffer
+    const int nchunks = (Tc + JB - 1) / JB;
+    int lo0 = 0, hi0 = -1, lo1 = 0, hi1 = -1;
+    const float* gsrc = nullptr;                     // row block of key tile j: gsrc + j * gstride
+    int64_t gstride = 0;
+    uint32_t rowbytes = 0;
+    bool issuer = false;
+    auto issue = [&](int c) {
+      const int j0 = c * JB, jn = min(JB, Tc - j0);
+      uint8_t* dst = sm + (c & 1) * JB * (kRowStride * 4);
+      if (!stats) {   // the slot already has the buffer's layout: one copy
+        mbar_expect_tx(&s_wbar[c & 1], (uint32_t)jn * kRowStride * 4u);
+        bulk_load(dst, gsrc + (int64_t)j0 * kRowStride, (uint32_t)jn * kRowStride * 4u,
+                  &s_wbar[c & 1]);
+      } else {
+        mbar_expect_tx(&s_wbar[c & 1], (uint32_t)jn * rowbytes);
+        for (int jj = 0; jj < jn; ++jj)
+          bulk_load(dst + jj * (kRowStride * 4), gsrc + (int64_t)(j0 + jj) * gstride, rowbytes,
+                    &s_wbar[c & 1]);
+      }
+    };
+    if (logw) {
+      key_tile_range(sh, 2 * pair, lo0, hi0);
+      if (ntile == 2) key_tile_range(sh, 2 * pair + 1, lo1, hi1);
+      gsrc = stats ? stats + bh * sh.T_c * sh.n_pad + pair * 256
+                   : (s_slot >= 0 ? scr.slots + (int64_t)s_slot * Tc * kRowStride : nullptr);
+      gstride = stats ? sh.n_pad : kRowStride;
+      rowbytes = (stats && ntile == 1) ? 512u : 1024u;
+      issuer = ww == 0 && lane == 0 && gsrc != nullptr;
+      fence_proxy_async_global();   // this thread's statistics, for the copies
+      named_sync(1, 256);           // every row's statistics are written
+      if (ww == 0 && lane == 0) {
+        s_wissued = issuer && mbar_wait(&bars.o_done[0], 0);
+        if (s_wissued) {
+          issue(0);
+          if (nchunks > 1) issue(1);
+        }
+      }
+    }
+    if (valid_tile) {
       // epilogue: O = acc / l, LSE = ln 2 (m + log2 l), once the last PV landed
       const bool done = __all_sync(0xffffffffu, ok && mbar_wait(&bars.o_done[t], 0));
       fence_after_sync();
@@ -378,77 +436,55 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       if (logw) s_lse[t * 128 + r] = lse_v;
     }
     if (logw) {
-      // Tile weights of the pair's query tiles: d_ij = max over the tile's
-      // rows r < n of fp32(LSE_{r,j} - LSE_r) (NaN if any term is NaN),
-      // clamped to <= 0 with -0 -> +0; key tiles outside tile i's attending
-      // range enter with LSE_{r,j} = -inf.  Every MMA has completed, so the
-      // dynamic shared memory is free: the pair's statistics rows (1 KB per
-      // key tile: 128 rows of each query tile) come in with bulk copies, in
-      // chunks of JB key tiles into two alternating buffers, while the eight
-      // softmax warps reduce the previous chunk, one warp per (query tile,
-      // key tile): a float4 of rows per lane, then shuffles.
-      fence_proxy_async_global();   // this thread's statistics, for the copies
-      named_sync(1, 256);
-      const int ww = warp - 4;                       // 0..7
-      constexpr int JB = C::BYTES / 2 / 1024;        // key tiles per buffer
-      const int nchunks = (Tc + JB - 1) / JB;
-      int lo0, hi0, lo1 = 0, hi1 = -1;
-      key_tile_range(sh, 2 * pair, lo0, hi0);
-      if (ntile == 2) key_tile_range(sh, 2 * pair + 1, lo1, hi1);
-      // row block of key tile j: gsrc + j * gstride floats
-      const float* gsrc = stats ? stats + bh * sh.T_c * sh.n_pad + pair * 256
-                                : (s_slot >= 0 ? scr.slots + (int64_t)s_slot * Tc * 256 : nullptr);
-      const int64_t gstride = stats ? sh.n_pad : 256;
-      const uint32_t rowbytes = (stats && ntile == 1) ? 512u : 1024u;
-      const bool issuer = ww == 0 && lane == 0 && gsrc != nullptr;
-      auto issue = [&](int c) {
-        const int j0 = c * JB, jn = min(JB, Tc - j0);
-        uint8_t* dst = sm + (c & 1) * JB * 1024;
-        mbar_expect_tx(&s_wbar[c & 1], (uint32_t)jn * rowbytes);
-        if (!stats) {
-          bulk_load(dst, gsrc + (int64_t)j0 * 256, (uint32_t)jn * 1024u, &s_wbar[c & 1]);
-        } else {
-          for (int jj = 0; jj < jn; ++jj)
-            bulk_load(dst + jj * 1024, gsrc + (int64_t)(j0 + jj) * gstride, rowbytes,
-                      &s_wbar[c & 1]);
-        }
-      };
-      if (issuer) {
-        issue(0);
-        if (nchunks > 1) issue(1);
-      }
+      named_sync(1, 256);            // every row's final LSE is in s_lse
       for (int c = 0; c < nchunks; ++c) {
         const int j0 = c * JB, jn = min(JB, Tc - j0);
-        const bool have = gsrc != nullptr && mbar_wait(&s_wbar[c & 1], (c >> 1) & 1);
-        const float* buf = reinterpret_cast<const float*>(sm + (c & 1) * JB * 1024);
-        for (int tt = 0; tt < ntile; ++tt) {
-          const int lo = tt ? lo1 : lo0, hi = tt ? hi1 : hi0;
-          const int r0 = (2 * pair + tt) * 128 + 4 * lane;
-          const float* l4 = s_lse + tt * 128 + 4 * lane;
-          float* wrow = logw + (bh * sh.T_r + 2 * pair + tt) * (int64_t)Tc;
-          for (int jj = ww; jj < jn; jj += 8) {
-            const int j = j0 + jj;
-            float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (j >= lo && j <= hi)
-              v = have ? reinterpret_cast<const float4*>(buf + jj * 256 + tt * 128)[lane]
-                       : make_float4(__uint_as_float(0x7fc00000u), 0.f, 0.f, 0.f);
-            float mx = -INFINITY;
-            if (r0 < sh.n) mx = max_nan(mx, __fsub_rn(v.x, l4[0]));
-            if (r0 + 1 < sh.n) mx = max_nan(mx, __fsub_rn(v.y, l4[1]));
-            if (r0 + 2 < sh.n) mx = max_nan(mx, __fsub_rn(v.z, l4[2]));
-            if (r0 + 3 < sh.n) mx = max_nan(mx, __fsub_rn(v.w, l4[3]));
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-              mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            if (lane == 0) {
-              float dv = isnan(mx) ? __uint_as_float(0x7fc00000u) : fminf(mx, 0.f);
-              if (dv == 0.f) dv = 0.f;   // -0 -> +0
-              wrow[j] = dv;
+        const bool have = s_wissued && mbar_wait(&s_wbar[c & 1], (c >> 1) & 1);
+        const float* buf = reinterpret_cast<const float*>(sm + (c & 1) * JB * (kRowStride * 4));
+        // tasks: (query tile, 32 consecutive key tiles of the chunk)
+        const int ngrp = (jn + 31) / 32;
+        for (int task = ww; task < ntile * ngrp; task += 8) {
+          const int tt = task / ngrp, jl = (task - tt * ngrp) * 32 + lane;
+          const int j = j0 + jl;
+          const int nv = min(128, sh.n - (2 * pair + tt) * 128);   // valid rows
+          const bool in = jl < jn && j >= (tt ? lo1 : lo0) && j <= (tt ? hi1 : hi0);
+          const float* src = buf + jl * kRowStride + tt * 128;
+          const float* lp = s_lse + tt * 128;
+          const float ninf = -INFINITY, qnan = __uint_as_float(0x7fc00000u);
+          const float4 fill = have ? make_float4(ninf, ninf, ninf, ninf)
+                                   : make_float4(qnan, qnan, qnan, qnan);
+          float m0 = ninf, m1 = ninf, m2 = ninf, m3 = ninf;
+          if (nv == 128) {           // a whole tile: no row checks
+#pragma unroll 8
+            for (int r4 = 0; r4 < 128; r4 += 4) {
+              const float4 v = (in && have) ? *reinterpret_cast<const float4*>(src + r4)
+                                            : (in ? fill : make_float4(ninf, ninf, ninf, ninf));
+              const float4 l = *reinterpret_cast<const float4*>(lp + r4);
+              m0 = max_nan(m0, __fsub_rn(v.x, l.x));
+              m1 = max_nan(m1, __fsub_rn(v.y, l.y));
+              m2 = max_nan(m2, __fsub_rn(v.z, l.z));
+              m3 = max_nan(m3, __fsub_rn(v.w, l.w));
             }
+          } else {
+            for (int r4 = 0; r4 < nv; r4 += 4) {
+              const float4 v = (in && have) ? *reinterpret_cast<const float4*>(src + r4)
+                                            : (in ? fill : make_float4(ninf, ninf, ninf, ninf));
+              const float4 l = *reinterpret_cast<const float4*>(lp + r4);
+              m0 = max_nan(m0, __fsub_rn(v.x, l.x));
+              if (r4 + 1 < nv) m1 = max_nan(m1, __fsub_rn(v.y, l.y));
+              if (r4 + 2 < nv) m2 = max_nan(m2, __fsub_rn(v.z, l.z));
+              if (r4 + 3 < nv) m3 = max_nan(m3, __fsub_rn(v.w, l.w));
+            }
+          }
+          if (jl < jn) {
+            const float mx = max_nan(max_nan(m0, m1), max_nan(m2, m3));
+            float dv = isnan(mx) ? qnan : fminf(mx, 0.f);
+            if (dv == 0.f) dv = 0.f;   // -0 -> +0
+            logw[(bh * sh.T_r + 2 * pair + tt) * (int64_t)Tc + j] = dv;
           }
         }
         named_sync(1, 256);          // every warp is done with this buffer
-        if (issuer && c + 2 < nchunks) issue(c + 2);
+        if (issuer && s_wissued && c + 2 < nchunks) issue(c + 2);
       }
     }
   }
@@ -513,7 +549,7 @@ size_t fwd_scratch_bytes(const Shape& sh) {
   const int ns = sh.d == 128 ? resident_ctas<128>() : resident_ctas<64>();
   if (ns <= 0) return 0;
   const size_t locks = ((size_t)ns * sizeof(int32_t) + 255) & ~(size_t)255;
-  return locks + (size_t)ns * sh.T_c * 256 * sizeof(float);
+  return locks + (size_t)ns * sh.T_c * kRowStride * sizeof(float);
 }
 
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,

@@ -159,9 +159,10 @@ bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats,
  * ------------------------------------------------------------------------- */
 
 /* Bytes of scratch bl_attn_fwd_tile_weights needs when tile_stats is NULL:
- * one slot of 256 * T_c floats for every forward CTA that can be resident on
- * the CURRENT device at once (about 152 * 256 * T_c * 4 bytes on a GB300),
- * plus one lock word per slot.  0 for an invalid or unsupported shape. */
+ * one slot of 260 * T_c floats for every forward CTA that can be resident on
+ * the CURRENT device at once (about 152 * 260 * T_c * 4 bytes on a GB300:
+ * 40 MB at T_c = 256, 162 MB at T_c = 1024), plus one lock word per slot.
+ * 0 for an invalid or unsupported shape. */
 size_t bl_fwd_workspace_bytes(const bl_shape* shape);
 
 /* bl_attn_fwd that also writes tile_logw (above).
