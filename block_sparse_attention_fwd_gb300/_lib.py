@@ -30,7 +30,15 @@ EXPORTS = ("bl_tile_stats_elems", "bl_lists_elems", "bl_bwd_workspace_bytes", "b
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("n", ctypes.c_int), ("H", ctypes.c_int),
                 ("Hk", ctypes.c_int), ("d", ctypes.c_int), ("block_q", ctypes.c_int),
-                ("block_k", ctypes.c_int), ("causal", ctypes.c_int), ("window", ctypes.c_int)]
+                ("block_k", ctypes.c_int), ("causal", ctypes.c_int), ("window", ctypes.c_int),
+                ("q_strides", ctypes.c_int64 * 4), ("k_strides", ctypes.c_int64 * 4),
+                ("v_strides", ctypes.c_int64 * 4), ("o_strides", ctypes.c_int64 * 4)]
+
+    def strides_of(self, role):
+        """Element strides a tensor of this role (q, k, v, o) must have, or None
+        when the shape's are all zero (a contiguous tensor)."""
+        st = tuple(getattr(self, role + "_strides"))
+        return st if any(st) else None
 
 
 class Lists(ctypes.Structure):
@@ -133,19 +141,43 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _need(t, dtype, shape, name):
+def _need(t, dtype, shape, name, strides=None):
+    """Checks a tensor argument.  strides: the element strides a BSHD view must
+    have (from the bl_shape); None means contiguous."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    if strides is None:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    elif any(sz > 1 and a != b for sz, a, b in zip(t.shape, t.stride(), strides)) or \
+            t.stride()[-1] != 1:
+        raise ValueError(f"{name} has strides {tuple(t.stride())}, the shape says {strides}")
 
 
 def make_shape(B, n, H, Hk, d, block_q, block_k, causal=0, window=0) -> Shape:
+    """A shape for contiguous BSHD tensors (all strides zero)."""
     return Shape(B, n, H, Hk, d, block_q, block_k, int(causal), int(window))
+
+
+def with_strides(shape: Shape, q=None, k=None, v=None, o=None) -> Shape:
+    """A copy of `shape` whose strides are those of the given BSHD views (q for
+    q/g_q, k for k/g_k, v for v/g_v, o for o/g_o); roles not given stay as they
+    are.  Every view must have a contiguous last dim."""
+    out = Shape.from_buffer_copy(shape)
+    for role, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t is None:
+            continue
+        st = tuple(int(x) for x in t.stride())
+        if len(st) != 4 or st[3] != 1:
+            raise ValueError(f"{role}: a BSHD view with a contiguous last dim is needed")
+        arr = getattr(out, role + "_strides")
+        for i, x in enumerate(st):
+            arr[i] = x
+    return out
 
 
 def tiles(shape: Shape):
@@ -171,10 +203,10 @@ def bwd_workspace_bytes(shape: Shape) -> int:
 
 def attn_fwd(shape, q, k, v, scale, o, lse, tile_stats=None):
     B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
-    _need(q, torch.bfloat16, (B, n, H, d), "q")
-    _need(k, torch.bfloat16, (B, n, Hk, d), "k")
-    _need(v, torch.bfloat16, (B, n, Hk, d), "v")
-    _need(o, torch.bfloat16, (B, n, H, d), "o")
+    _need(q, torch.bfloat16, (B, n, H, d), "q", shape.strides_of("q"))
+    _need(k, torch.bfloat16, (B, n, Hk, d), "k", shape.strides_of("k"))
+    _need(v, torch.bfloat16, (B, n, Hk, d), "v", shape.strides_of("v"))
+    _need(o, torch.bfloat16, (B, n, H, d), "o", shape.strides_of("o"))
     _need(lse, torch.float32, (B, H, n), "lse")
     if tile_stats is not None:
         T_r, T_c = tiles(shape)
@@ -196,10 +228,10 @@ def attn_fwd_tile_weights(shape, q, k, v, scale, o, lse, tile_logw, tile_stats=N
     only in `workspace` (uint8, at least fwd_workspace_bytes)."""
     B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
     T_r, T_c = tiles(shape)
-    _need(q, torch.bfloat16, (B, n, H, d), "q")
-    _need(k, torch.bfloat16, (B, n, Hk, d), "k")
-    _need(v, torch.bfloat16, (B, n, Hk, d), "v")
-    _need(o, torch.bfloat16, (B, n, H, d), "o")
+    _need(q, torch.bfloat16, (B, n, H, d), "q", shape.strides_of("q"))
+    _need(k, torch.bfloat16, (B, n, Hk, d), "k", shape.strides_of("k"))
+    _need(v, torch.bfloat16, (B, n, Hk, d), "v", shape.strides_of("v"))
+    _need(o, torch.bfloat16, (B, n, H, d), "o", shape.strides_of("o"))
     _need(lse, torch.float32, (B, H, n), "lse")
     _need(tile_logw, torch.float32, (B, H, T_r, T_c), "tile_logw")
     if tile_stats is not None:
@@ -266,13 +298,18 @@ def mask_from_stats(shape, tile_stats, lse, negl_prob, lists):
     _check("bl_mask_from_stats", code)
 
 
+def _bwd_tensors(shape, q, k, v, o, g_o, g_q, g_k, g_v):
+    B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
+    for t, nm, sh, role in ((q, "q", (B, n, H, d), "q"), (k, "k", (B, n, Hk, d), "k"),
+                            (v, "v", (B, n, Hk, d), "v"), (o, "o", (B, n, H, d), "o"),
+                            (g_o, "g_o", (B, n, H, d), "o"), (g_q, "g_q", (B, n, H, d), "q"),
+                            (g_k, "g_k", (B, n, Hk, d), "k"), (g_v, "g_v", (B, n, Hk, d), "v")):
+        _need(t, torch.bfloat16, sh, nm, shape.strides_of(role))
+
+
 def attn_bwd(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, workspace):
     B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
-    for t, nm, sh in ((q, "q", (B, n, H, d)), (k, "k", (B, n, Hk, d)), (v, "v", (B, n, Hk, d)),
-                      (o, "o", (B, n, H, d)), (g_o, "g_o", (B, n, H, d)),
-                      (g_q, "g_q", (B, n, H, d)), (g_k, "g_k", (B, n, Hk, d)),
-                      (g_v, "g_v", (B, n, Hk, d))):
-        _need(t, torch.bfloat16, sh, nm)
+    _bwd_tensors(shape, q, k, v, o, g_o, g_q, g_k, g_v)
     _need(lse, torch.float32, (B, H, n), "lse")
     if workspace.dtype != torch.uint8 or not workspace.is_cuda:
         raise TypeError("workspace must be a CUDA uint8 tensor")
@@ -299,11 +336,7 @@ def attn_bwd_noalloc(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v):
     """bl_attn_bwd_noalloc: the backward with the library's fixed device scratch
     instead of a workspace (for callers that cannot allocate device memory)."""
     B, n, H, Hk, d = shape.B, shape.n, shape.H, shape.Hk, shape.d
-    for t, nm, sh in ((q, "q", (B, n, H, d)), (k, "k", (B, n, Hk, d)), (v, "v", (B, n, Hk, d)),
-                      (o, "o", (B, n, H, d)), (g_o, "g_o", (B, n, H, d)),
-                      (g_q, "g_q", (B, n, H, d)), (g_k, "g_k", (B, n, Hk, d)),
-                      (g_v, "g_v", (B, n, Hk, d))):
-        _need(t, torch.bfloat16, sh, nm)
+    _bwd_tensors(shape, q, k, v, o, g_o, g_q, g_k, g_v)
     _need(lse, torch.float32, (B, H, n), "lse")
     ls = _lists_struct(lists) if lists is not None else None
     code = load().bl_attn_bwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o),

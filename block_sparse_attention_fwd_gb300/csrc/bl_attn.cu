@@ -29,6 +29,30 @@ bl_status check_shape(const bl_shape* s, Shape* out) {
   sh.T_r = (s->n + s->block_q - 1) / s->block_q;
   sh.T_c = (s->n + s->block_k - 1) / s->block_k;
   sh.n_pad = (int64_t)sh.T_r * s->block_q;
+  // strides: all zero means contiguous BSHD; otherwise the d stride is 1 and
+  // the others are positive multiples of 8 elements (16 bytes, for TMA)
+  sh.strided = false;
+  const int64_t* in[4] = {s->q_strides, s->k_strides, s->v_strides, s->o_strides};
+  int64_t* dst[4] = {sh.qs, sh.ks, sh.vs, sh.os};
+  const int heads[4] = {s->H, s->Hk, s->Hk, s->H};
+  for (int t = 0; t < 4; ++t) {
+    const int64_t* st = in[t];
+    if (st[0] == 0 && st[1] == 0 && st[2] == 0 && st[3] == 0) {
+      dst[t][2] = s->d;
+      dst[t][1] = (int64_t)heads[t] * s->d;
+      dst[t][0] = (int64_t)s->n * heads[t] * s->d;
+      continue;
+    }
+    if (st[3] != 1) return BL_ERR_INVALID_ARG;
+    for (int k = 0; k < 3; ++k) {
+      if (st[k] <= 0 || st[k] % 8 != 0) return BL_ERR_INVALID_ARG;
+      dst[t][k] = st[k];
+    }
+    if (dst[t][2] < s->d) return BL_ERR_INVALID_ARG;   // rows of one head may not overlap
+    if (dst[t][2] != s->d || dst[t][1] != (int64_t)heads[t] * s->d ||
+        dst[t][0] != (int64_t)s->n * heads[t] * s->d)
+      sh.strided = true;
+  }
   *out = sh;
   return BL_OK;
 }
@@ -102,7 +126,7 @@ bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats, con
 
 size_t bl_fwd_workspace_bytes(const bl_shape* shape) {
   bl::Shape sh;
-  if (check_shape(shape, &sh) != BL_OK || !bl::fwd_tc_supported(sh) || sh.T_c > 2048) return 0;
+  if (check_shape(shape, &sh) != BL_OK || !bl::fwd_tile_weights_supported(sh)) return 0;
   return bl::fwd_scratch_bytes(sh);
 }
 
@@ -118,7 +142,7 @@ bl_status bl_attn_fwd_tile_weights(const bl_shape* shape, const void* q, const v
       !aligned16(tile_logw) || (tile_stats && !aligned16(tile_stats)))
     return BL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
-  if (!bl::fwd_tc_supported(sh) || sh.T_c > 2048) return BL_ERR_UNSUPPORTED;
+  if (!bl::fwd_tile_weights_supported(sh)) return BL_ERR_UNSUPPORTED;
   if (!tile_stats) {
     const size_t need = bl::fwd_scratch_bytes(sh);
     if (need == 0) return BL_ERR_CUDA;
@@ -158,6 +182,7 @@ bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k, const
     if (!p || !aligned16(p)) return BL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
   if (lists && (!lists->q_idx || !lists->q_cnt)) return BL_ERR_INVALID_ARG;
+  if (sh.strided && !bl::bwd_tc_supported(sh)) return BL_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace)) return BL_ERR_WORKSPACE;
   if (workspace_bytes < bl_bwd_workspace_bytes(shape)) return BL_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -54,8 +54,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       *reinterpret_cast<float2*>(z) = make_float2(0.f, 0.f);
   }
   constexpr int E = D / 32;  // elements per lane (2 or 4)
-  const __nv_bfloat16* op = o + row * D + lane * E;
-  const __nv_bfloat16* gp = g_o + row * D + lane * E;
+  const int rh = (int)(row % sh.H);
+  const int64_t rbr = row / sh.H;
+  const int64_t ro = bshd(sh.os, (int)(rbr / sh.n), (int)(rbr % sh.n), rh);
+  const __nv_bfloat16* op = o + ro + lane * E;
+  const __nv_bfloat16* gp = g_o + ro + lane * E;
   float acc = 0.f;
 #pragma unroll
   for (int e = 0; e < E; e += 2) {
@@ -281,17 +284,26 @@ __global__ void __launch_bounds__(BK * 2) bwd_dkdv_kernel(
   }
 }
 
-// G_Q = bf16(s * dq_acc)
+// G_Q = bf16(s * dq_acc); with STRIDED, G_Q has the strides sh.qs (the
+// accumulator is contiguous [B,n,H,d]).
+template <bool STRIDED>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc,
                                                          uint2* __restrict__ g_q, int64_t n4,
-                                                         float scale) {
+                                                         float scale, Shape sh) {
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4;
        x += (int64_t)gridDim.x * blockDim.x) {
     float4 a = acc[x];
     uint2 r;
     r.x = pack_bf16(a.x * scale, a.y * scale);
     r.y = pack_bf16(a.z * scale, a.w * scale);
-    g_q[x] = r;
+    if constexpr (STRIDED) {
+      const int64_t e = x * 4, row = e / sh.d, br = row / sh.H;
+      const int64_t off = bshd(sh.qs, (int)(br / sh.n), (int)(br % sh.n), (int)(row % sh.H)) +
+                          e % sh.d;
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(g_q) + off) = r;
+    } else {
+      g_q[x] = r;
+    }
   }
 }
 
@@ -348,7 +360,12 @@ cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void
   const int64_t n4 = rows * sh.d / 4;
   unsigned cblocks = (unsigned)((n4 + 255) / 256);
   if (cblocks > 152u * 16u) cblocks = 152u * 16u;
-  dq_convert_kernel<<<cblocks, 256, 0, st>>>((const float4*)ws_dq, (uint2*)g_q, n4, scale);
+  if (sh.strided)
+    dq_convert_kernel<true><<<cblocks, 256, 0, st>>>((const float4*)ws_dq, (uint2*)g_q, n4, scale,
+                                                     sh);
+  else
+    dq_convert_kernel<false><<<cblocks, 256, 0, st>>>((const float4*)ws_dq, (uint2*)g_q, n4,
+                                                      scale, sh);
   return cudaGetLastError();
 }
 

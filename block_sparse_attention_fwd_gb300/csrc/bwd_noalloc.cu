@@ -64,6 +64,7 @@ extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, c
 
   bl::Shape sh;
   if (bl::check_shape(shape, &sh) != BL_OK) return BL_ERR_INVALID_ARG;  // unreachable: need > 0
+  if (sh.strided && !bl::bwd_tc_supported(sh)) return BL_ERR_UNSUPPORTED;
   // Same layout as the workspace of bl_attn_bwd.  The preprocessing kernel
   // that launch_bwd runs first writes every D entry and zeroes the dQ
   // accumulator and the status word, so nothing left by an earlier call leaks

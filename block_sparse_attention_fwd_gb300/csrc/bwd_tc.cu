@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       } else {
         const int row = ie.j * 128 + r;
         uint4* dst = reinterpret_cast<uint4*>(
-            (half == 0 ? g_v : g_k) + (((int64_t)ie.b * sh.n + row) * sh.Hk + ie.hk) * D);
+            half == 0 ? g_v + bshd(sh.vs, ie.b, row, ie.hk) : g_k + bshd(sh.ks, ie.b, row, ie.hk));
         if (row < sh.n) {
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -809,12 +809,12 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
                      float scale, cudaStream_t st) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv, mg, md, mgk, mgv;
-  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
-      !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 128) ||
-      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) ||
-      !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128) ||
-      !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 32) ||
-      !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 32) ||
+  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128, sh.qs) ||
+      !make_bshd_map(&mg, g_o, sh.B, sh.n, sh.H, D, 128, sh.os) ||
+      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128, sh.ks) ||
+      !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128, sh.vs) ||
+      !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 32, sh.ks) ||
+      !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 32, sh.vs) ||
       !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;

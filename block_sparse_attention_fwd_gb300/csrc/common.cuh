@@ -15,7 +15,16 @@ struct Shape {
   int T_r, T_c;
   int64_t n_pad;  // T_r * block_q
   int causal, window;
+  // element strides of the batch, sequence and head dims (the d stride is 1)
+  // of q and g_q (qs), k and g_k (ks), v and g_v (vs), o and g_o (os)
+  int64_t qs[3], ks[3], vs[3], os[3];
+  bool strided;   // some tensor is not contiguous BSHD
 };
+
+// Element offset of (batch b, row r, head h) in a BSHD tensor with strides s.
+__host__ __device__ __forceinline__ int64_t bshd(const int64_t (&s)[3], int b, int r, int h) {
+  return (int64_t)b * s[0] + (int64_t)r * s[1] + (int64_t)h * s[2];
+}
 
 // Key tiles [lo, hi] of query tile i that hold at least one attending
 // (query, key) pair under the causal / sliding-window structure: causal keeps

@@ -1,5 +1,8 @@
 // Attention forward with per-(query row, key tile) LSE statistics on tcgen05
-// tensor cores (sm_103a), 128 x 128 tiles, head dim 64 or 128.
+// tensor cores (sm_103a), head dim 64 or 128.  The MMA tiles are 128 query
+// rows x 128 keys whatever the statistics' tile sizes: with 64-key tiles the
+// two halves of each S row are summed separately, one statistic each, and
+// with 64-row query tiles the statistics rows are simply stored as rows.
 //
 // Math: "Introducing BackLite", Backpropagation for attention (S = s Q K^T,
 // P = softmax_row(S), O = P V, computed exactly, Using Sparsity); "BackLite"
@@ -86,7 +89,9 @@ struct RowScratch {
   int nslots;
 };
 
-template <int D>
+// SUB: statistics per 128-key MMA tile (1 for 128-key tiles, 2 for 64-key
+// tiles, whose two halves of the S row are summed separately).
+template <int D, int SUB>
 __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
@@ -109,15 +114,20 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   const int pair = (sh.causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
   const int h = blockIdx.y, b = blockIdx.z;
   const int hk = h / (sh.H / sh.Hk);
-  const int Tc = sh.T_c;
+  const int Tc = sh.T_c;                  // statistics key tiles (block_k wide)
+  const int Tq = (sh.n + 127) / 128;      // 128-row query tiles (the MMA's rows)
   // the second tile of the last pair may lie wholly past the last query tile
-  const int ntile = min(2, sh.T_r - 2 * pair);
-  // key tiles [j_lo, j_hi] hold an attending pair for tile A or tile B; the
-  // rings and barrier phases count visits jj = j - j_lo
-  int j_lo, j_hi, lo_b, hi_b;
-  key_tile_range(sh, 2 * pair, j_lo, j_hi);
-  key_tile_range(sh, 2 * pair + ntile - 1, lo_b, hi_b);
-  j_hi = hi_b;
+  const int ntile = min(2, Tq - 2 * pair);
+  // 128-key tiles [j_lo, j_hi] hold an attending pair for tile A or tile B;
+  // the rings and barrier phases count visits jj = j - j_lo.  Causal and
+  // window structure come with 128 x 128 tiles only.
+  int j_lo = 0, j_hi = (sh.n + 127) / 128 - 1;
+  if (sh.causal || sh.window) {
+    int lo_b, hi_b;
+    key_tile_range(sh, 2 * pair, j_lo, j_hi);
+    key_tile_range(sh, 2 * pair + ntile - 1, lo_b, hi_b);
+    j_hi = hi_b;
+  }
   const int nj = j_hi - j_lo + 1;
 
   if (threadIdx.x == 0) {
@@ -309,20 +319,36 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
       // a row that has attended no key yet keeps m = -inf: its p are 0
       const float m_sub = m_new == -INFINITY ? 0.f : m_new;
-      float ts = 0.f;
+      float ts = 0.f, ts_lo = 0.f;
       // p = 2^(x s log2 e - m); bf16 pairs packed in place (entry c from 2c, 2c+1)
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), scale_log2, -m_sub));
         const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), scale_log2, -m_sub));
+        if (SUB == 2 && c == 32) {   // keys 0-63 and 64-127: two 64-key tiles
+          ts_lo = ts;
+          ts = 0.f;
+        }
         ts += p0 + p1;
         x[c] = pack_bf16(p0, p1);
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         tmem_st16(s_col + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&x[c * 16]));
-      if (st_row)
-        st_row[(int64_t)j * st_stride] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
+      if constexpr (SUB == 1) {
+        if (st_row)
+          st_row[(int64_t)j * st_stride] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
+      } else {
+        // rows past the statistics' T_r * block_q rows are not stored
+        if (st_row && row < sh.n_pad) {
+          st_row[(int64_t)(2 * j) * st_stride] =
+              row < sh.n ? (m_new + __log2f(ts_lo)) * kLn2 : -INFINITY;
+          if (2 * j + 1 < Tc)
+            st_row[(int64_t)(2 * j + 1) * st_stride] =
+                row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
+        }
+        ts += ts_lo;
+      }
       l_run = l_run * alpha + ts;
       m_ref = m_new;
       // rescale O in TMEM (rare).  S_t(jj) has completed, hence so has
@@ -346,7 +372,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     if (valid_tile) {
       if (!ok && lane == 0) fail();
       // key tiles this pair never visits carry no weight for this row
-      if (stats) {
+      if (SUB == 1 && stats) {
         for (int j = 0; j < j_lo; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
         for (int j = j_hi + 1; j < Tc; ++j) st_row[(int64_t)j * sh.n_pad] = -INFINITY;
       }
@@ -409,7 +435,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       const bool done = __all_sync(0xffffffffu, ok && mbar_wait(&bars.o_done[t], 0));
       fence_after_sync();
       const float inv = 1.f / l_run;
-      __nv_bfloat16* orow = o + (((int64_t)b * sh.n + row) * sh.H + h) * D;
+      __nv_bfloat16* orow = o + bshd(sh.os, b, row, h);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
@@ -498,25 +524,25 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   }
 }
 
-template <int D>
+template <int D, int SUB>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                      float* lse, float* stats, float* logw, RowScratch scr, float scale,
                      cudaStream_t st) {
   using C = FCfg<D>;
   CUtensorMap mq, mk, mv;
-  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128) ||
-      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128) ||
-      !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128))
+  if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128, sh.qs) ||
+      !make_bshd_map(&mk, k, sh.B, sh.n, sh.Hk, D, 128, sh.ks) ||
+      !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128, sh.vs))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
-  auto kern = fwd_tc_kernel<D>;
+  auto kern = fwd_tc_kernel<D, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (scr.locks) {
     e = cudaMemsetAsync(scr.locks, 0, (size_t)scr.nslots * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid((sh.T_r + 1) / 2, sh.H, sh.B);
+  dim3 grid(((sh.n + 127) / 128 + 1) / 2, sh.H, sh.B);
   kern<<<grid, 384, smem, st>>>(mq, mk, mv, (__nv_bfloat16*)o, lse, stats, logw, scr, sh,
                                 scale * kLog2e);
   return cudaGetLastError();
@@ -527,7 +553,7 @@ template <int D>
 int resident_ctas() {
   using C = FCfg<D>;
   const int smem = C::BYTES + 1024;
-  auto kern = fwd_tc_kernel<D>;
+  auto kern = fwd_tc_kernel<D, 1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
@@ -542,7 +568,13 @@ int resident_ctas() {
 }  // namespace
 
 bool fwd_tc_supported(const Shape& sh) {
-  return sh.block_q == 128 && sh.block_k == 128 && (sh.d == 64 || sh.d == 128);
+  return (sh.block_q == 64 || sh.block_q == 128) && (sh.block_k == 64 || sh.block_k == 128) &&
+         (sh.d == 64 || sh.d == 128);
+}
+
+bool fwd_tile_weights_supported(const Shape& sh) {
+  return sh.block_q == 128 && sh.block_k == 128 && (sh.d == 64 || sh.d == 128) &&
+         sh.T_c <= 2048;
 }
 
 size_t fwd_scratch_bytes(const Shape& sh) {
@@ -564,8 +596,19 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
     scr.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + locks);
     scr.nslots = ns;
   }
-  if (sh.d == 128) return launch_t<128>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
-  return launch_t<64>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+  if (sh.block_k == 64) {
+    if (logw) return cudaErrorInvalidValue;   // tile weights need 128 x 128 tiles
+    if (sh.d == 128) return launch_t<128, 2>(sh, q, k, v, o, lse, stats, nullptr, scr, scale, st);
+    return launch_t<64, 2>(sh, q, k, v, o, lse, stats, nullptr, scr, scale, st);
+  }
+  if (sh.d == 128) return launch_t<128, 1>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+  return launch_t<64, 1>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+}
+
+cudaError_t launch_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o,
+                       float* lse, float* stats, float scale, cudaStream_t st) {
+  if (!fwd_tc_supported(sh)) return cudaErrorInvalidValue;
+  return launch_fwd_tc(sh, q, k, v, o, lse, stats, nullptr, nullptr, scale, st);
 }
 
 }  // namespace bl

@@ -40,6 +40,7 @@ cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const v
 // 128).  logw != nullptr also writes the tile weights [B,H,T_r,T_c]; with
 // stats == nullptr their rows go through `scratch` (fwd_scratch_bytes).
 bool fwd_tc_supported(const Shape& sh);
+bool fwd_tile_weights_supported(const Shape& sh);
 size_t fwd_scratch_bytes(const Shape& sh);
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                           float* lse, float* stats, float* logw, void* scratch, float scale,
@@ -52,9 +53,11 @@ cudaError_t launch_grad_error(const void* a, const void* b, int64_t n, double* o
 cudaError_t launch_combine(int parts, int B, int n, int H, int d, const void* o_parts,
                            const float* lse_parts, void* o, float* lse, cudaStream_t st);
 
-// 4-D TMA map of a BSHD bf16 tensor [B][n][heads][d]: box of 64 elements of d
-// x 1 head x `rows` tokens x 1 batch, 128-byte swizzle, out-of-range reads 0.
-bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows);
+// 4-D TMA map of a BSHD bf16 tensor [B][n][heads][d] with element strides
+// st = {batch, seq, head} (d contiguous): box of 64 elements of d x 1 head x
+// `rows` tokens x 1 batch, 128-byte swizzle, out-of-range reads 0.
+bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows,
+                   const int64_t* st);
 
 // The same for an fp32 BSHD tensor, box of 32 elements of d (128 bytes) x 1
 // head x `rows` tokens, 128-byte swizzle: the target of dQ reduce-adds.

@@ -1,6 +1,7 @@
 // TMA tensor maps for BSHD bf16 tensors (host side).
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "kernels.h"
 
@@ -30,12 +31,12 @@ EncodeFn encode_fn() {
 
 }  // namespace
 
-bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows) {
+bool make_bshd_map(CUtensorMap* m, const void* base, int B, int n, int heads, int d, int rows,
+                   const int64_t* st) {
   EncodeFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)n, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
-                           (cuuint64_t)n * heads * d * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
   cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,

@@ -9,12 +9,32 @@ ranks) for reporting.
 from __future__ import annotations
 
 
-def shard_groups(B: int, Hk: int, rank: int, world: int):
-    """The (batch, kv head) groups rank `rank` of `world` owns: round-robin over
-    the B*Hk groups in (b, hk) order, so every group has exactly one owner."""
+def _block(count: int, rank: int, world: int):
+    """[lo, hi) of rank's balanced contiguous block of `count` items."""
+    base, extra = divmod(count, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def shard_slices(B: int, Hk: int, rank: int, world: int):
+    """The rectangle of (batch, kv head) groups rank `rank` of `world` owns:
+    ((b0, b1), (hk0, hk1)).  Kv heads are split into balanced contiguous blocks
+    when there are at least as many as ranks, batches otherwise, so a rank's
+    share of every tensor is one slice -- q[b0:b1, :, hk0*G:hk1*G] and
+    k[b0:b1, :, hk0:hk1] with G = H / Hk -- that the library takes as a strided
+    view (bl_shape strides), with no gather.  Every group has exactly one
+    owner; a rank may own none when there are more ranks than groups."""
     if world < 1 or not (0 <= rank < world):
         raise ValueError("bad rank/world")
-    return [divmod(u, Hk) for u in range(rank, B * Hk, world)]
+    if Hk >= world:
+        return (0, B), _block(Hk, rank, world)
+    return _block(B, rank, world), (0, Hk)
+
+
+def shard_groups(B: int, Hk: int, rank: int, world: int):
+    """The (batch, kv head) groups of shard_slices, in (b, hk) order."""
+    (b0, b1), (h0, h1) = shard_slices(B, Hk, rank, world)
+    return [(b, hk) for b in range(b0, b1) for hk in range(h0, h1)]
 
 
 def max_over_ranks(value: float, device=None) -> float:

@@ -14,8 +14,9 @@
  *                       Backpropagation for attention, and Using Sparsity).
  *
  * Tensors
- *   q, o, g_o, g_q : [B, n, H,  d] bf16, contiguous (batch, seq, head, dim)
- *   k, v, g_k, g_v : [B, n, Hk, d] bf16, contiguous; query head h reads kv
+ *   q, o, g_o, g_q : [B, n, H,  d] bf16 (batch, seq, head, dim), contiguous
+ *                    unless bl_shape gives strides
+ *   k, v, g_k, g_v : [B, n, Hk, d] bf16, likewise; query head h reads kv
  *                    head h / (H / Hk) (grouped-query attention, README,
  *                    Forward signature: key/value carry heads_k heads).
  *   lse            : [B, H, n] fp32, natural log: LSE_r = log sum_c exp(s q_r.k_c)
@@ -66,6 +67,15 @@ typedef struct {
   int B, n, H, Hk, d;
   int block_q, block_k;
   int causal, window;
+  /* Element strides of the four BSHD dims [batch, seq, head, dim], for
+   * tensors that are views of larger ones (a kv-head slice of a batch, a
+   * fused QKV projection): q_strides for q and g_q, k_strides for k and g_k,
+   * v_strides for v and g_v, o_strides for o and g_o.  All four entries 0
+   * (what a zero-initialised struct holds) means contiguous BSHD.  Otherwise
+   * the dim stride is 1, the others positive multiples of 8 (16 bytes), and
+   * the head stride at least d.  Strided tensors need the tcgen05 backward
+   * (128 x 128 tiles); the packed (varlen) calls take contiguous tensors. */
+  int64_t q_strides[4], k_strides[4], v_strides[4], o_strides[4];
 } bl_shape;
 
 /* Block-sparse tile lists of one backward, all device memory.

@@ -247,11 +247,13 @@ C_PROGRAM = r"""
 #include "bl_attn.h"
 
 int main(void) {
-  bl_shape s = {1, 1000, 2, 1, 64, 128, 64, 0, 0};
+  bl_shape s, s2;
   int32_t cu[4] = {0, 100, 100, 356};
   bl_varlen v;
   bl_varlen_sizes z;
   bl_status st;
+  memset(&s, 0, sizeof s);
+  s.B = 1; s.n = 1000; s.H = 2; s.Hk = 1; s.d = 64; s.block_q = 128; s.block_k = 64;
   printf("%zu %zu\n", bl_tile_stats_elems(&s), bl_bwd_workspace_bytes(&s));
   memset(&v, 0, sizeof v);
   v.nseq = 3; v.cu_seqlens = cu; v.H = 4; v.Hk = 2; v.d = 64; v.block_q = 128; v.block_k = 128;
@@ -260,6 +262,13 @@ int main(void) {
          z.kv_cnt, z.q_idx, z.q_cnt, z.bwd_workspace_bytes, z.groups);
   printf("%d\n", (int)bl_attn_fwd(&s, NULL, NULL, NULL, 0.125f, NULL, NULL, NULL, NULL));
   printf("%s\n", bl_status_string(BL_ERR_UNSUPPORTED));
+  /* a kv-head slice view: strides of the full tensor; a last stride of 2 is refused */
+  s2 = s;
+  s2.q_strides[0] = 1000 * 8 * 64; s2.q_strides[1] = 8 * 64; s2.q_strides[2] = 64;
+  s2.q_strides[3] = 1;
+  printf("%zu", bl_tile_stats_elems(&s2));
+  s2.q_strides[3] = 2;
+  printf(" %zu\n", bl_tile_stats_elems(&s2));
   return 0;
 }
 """
@@ -296,6 +305,7 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     assert want[1:4] == [356, 4 * 356, 4 * 1 * 128 + 4 * 2 * 256] and want[-1] == 2
     assert lines[2] == "1"                           # BL_ERR_INVALID_ARG before any launch
     assert lines[3] == "unsupported configuration"
+    assert lines[4].split() == [lines[0].split()[0], "0"]
 
 
 def test_varlen_splits_runs_longer_than_the_grid_limit(lib):
@@ -359,3 +369,33 @@ def test_varlen_layout_matches_the_oracle_on_random_batches(lib):
         # a group is a run of consecutive sequences of one non-zero length (an
         # empty sequence ends a run)
         assert sz.groups == sum(1 for i, n in enumerate(lens) if n and (i == 0 or lens[i - 1] != n))
+
+
+def test_strided_shapes_are_validated_on_the_host(lib):
+    """bl_shape strides: zero means contiguous; otherwise the dim stride is 1,
+    the others positive multiples of 8 elements, the head stride at least d.
+    A strided backward needs 128 x 128 tiles (host check before any launch)."""
+    from block_sparse_attention_fwd_gb300 import _lib
+    base = _lib.make_shape(1, 1000, 4, 2, 64, 128, 128)
+    want = _lib.tile_stats_elems(base)
+
+    def with_q(st):
+        s = _lib.Shape.from_buffer_copy(base)
+        for i, x in enumerate(st):
+            s.q_strides[i] = x
+        return s
+
+    # a view of heads 4..7 of an [1, 1000, 16, 64] tensor
+    assert _lib.tile_stats_elems(with_q((1000 * 16 * 64, 16 * 64, 64, 1))) == want
+    for bad in ((1000 * 16 * 64, 16 * 64, 64, 2),     # dim stride must be 1
+                (1000 * 16 * 64, 16 * 64 + 4, 64, 1),  # not a multiple of 8
+                (1000 * 16 * 64, 16 * 64, 32, 1),      # heads overlap
+                (0, 16 * 64, 64, 1)):                  # non-positive
+        assert _lib.tile_stats_elems(with_q(bad)) == 0
+    s64 = _lib.make_shape(1, 1000, 4, 2, 64, 64, 64)
+    for i, x in enumerate((1000 * 16 * 64, 16 * 64, 64, 1)):
+        s64.q_strides[i] = x
+    ok = ctypes.c_void_p(0x10000)
+    r = lib.bl_attn_bwd(ctypes.byref(s64), ok, ok, ok, ok, ok, ok, 0.125, None, ok, ok, ok, ok,
+                        1 << 30, None)
+    assert r == 2                                   # BL_ERR_UNSUPPORTED

@@ -9,7 +9,7 @@ import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
-from block_sparse_attention_fwd_gb300.dist import max_over_ranks, shard_groups
+from block_sparse_attention_fwd_gb300.dist import max_over_ranks, shard_groups, shard_slices
 
 
 def _free_port():
@@ -25,6 +25,9 @@ def _worker(rank, world, port, B, Hk, out):
                             world_size=world)
     try:
         mine = shard_groups(B, Hk, rank, world)
+        (b0, b1), (h0, h1) = shard_slices(B, Hk, rank, world)
+        # the rank's slices hold exactly its groups
+        assert mine == [(b, h) for b in range(b0, b1) for h in range(h0, h1)]
         gathered = [None] * world
         dist.all_gather_object(gathered, mine)
         t = max_over_ranks(10.0 + rank)
@@ -33,7 +36,7 @@ def _worker(rank, world, port, B, Hk, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("B,Hk", [(1, 40), (2, 8), (3, 1)])
+@pytest.mark.parametrize("B,Hk", [(1, 40), (2, 8), (3, 1), (2, 5), (1, 1)])
 def test_two_gloo_ranks_partition_and_time(B, Hk):
     world = 2
     mgr = mp.get_context("spawn").Manager()
@@ -46,6 +49,16 @@ def test_two_gloo_ranks_partition_and_time(B, Hk):
         assert sorted(allg) == [(b, h) for b in range(B) for h in range(Hk)]
         assert len(allg) == len(set(allg))
         assert t == 11.0
+
+
+def test_shard_slices_are_balanced_blocks():
+    # kv heads split when there are enough, batches otherwise
+    assert [shard_slices(1, 40, r, 2) for r in range(2)] == [((0, 1), (0, 20)), ((0, 1), (20, 40))]
+    assert [shard_slices(2, 5, r, 2) for r in range(2)] == [((0, 2), (0, 3)), ((0, 2), (3, 5))]
+    assert [shard_slices(3, 1, r, 2) for r in range(2)] == [((0, 2), (0, 1)), ((2, 3), (0, 1))]
+    assert [shard_slices(1, 8, r, 3) for r in range(3)] == [((0, 1), (0, 3)), ((0, 1), (3, 6)),
+                                                           ((0, 1), (6, 8))]
+    assert shard_groups(1, 1, 1, 2) == []          # more ranks than groups: rank 1 idle
 
 
 def test_single_process_identity():
