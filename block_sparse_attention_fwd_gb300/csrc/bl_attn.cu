@@ -92,7 +92,7 @@ size_t bl_lists_elems(const bl_shape* shape, size_t out[5]) {
 size_t bl_bwd_workspace_bytes(const bl_shape* shape) {
   bl::Shape sh;
   if (check_shape(shape, &sh) != BL_OK) return 0;
-  return ws_D_bytes(sh) + ws_dq_bytes(sh) + bl::kWsStatusBytes;
+  return bl::ws_status_off(sh) + bl::kWsStatusBytes;
 }
 
 bl_status bl_attn_fwd(const bl_shape* shape, const void* q, const void* k, const void* v,
@@ -182,16 +182,17 @@ bl_status bl_attn_bwd(const bl_shape* shape, const void* q, const void* k, const
     if (!p || !aligned16(p)) return BL_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
   if (lists && (!lists->q_idx || !lists->q_cnt)) return BL_ERR_INVALID_ARG;
-  if (sh.strided && !bl::bwd_tc_supported(sh)) return BL_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace)) return BL_ERR_WORKSPACE;
   if (workspace_bytes < bl_bwd_workspace_bytes(shape)) return BL_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* ws_D = reinterpret_cast<float*>(ws);
   float* ws_dq = reinterpret_cast<float*>(ws + ws_D_bytes(sh));
-  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + ws_D_bytes(sh) + ws_dq_bytes(sh));
+  int32_t* ws_sub = reinterpret_cast<int32_t*>(ws + ws_D_bytes(sh) + ws_dq_bytes(sh));
+  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + bl::ws_status_off(sh));
   return cuda_status(bl::launch_bwd(sh, q, k, v, o, g_o, lse, scale,
                                     lists ? lists->q_idx : nullptr, lists ? lists->q_cnt : nullptr,
-                                    g_q, g_k, g_v, ws_D, ws_dq, ws_status, (cudaStream_t)stream));
+                                    g_q, g_k, g_v, ws_D, ws_dq, ws_sub, ws_status,
+                                    (cudaStream_t)stream));
 }
 
 bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace, void* stream) {
@@ -200,7 +201,7 @@ bl_status bl_bwd_check_status(const bl_shape* shape, const void* workspace, void
   if (s != BL_OK) return s;
   if (!workspace) return BL_ERR_WORKSPACE;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
-  const int32_t* st = reinterpret_cast<const int32_t*>(ws + ws_D_bytes(sh) + ws_dq_bytes(sh));
+  const int32_t* st = reinterpret_cast<const int32_t*>(ws + bl::ws_status_off(sh));
   int32_t host = 0;
   cudaError_t e = cudaMemcpyAsync(&host, st, sizeof(int32_t), cudaMemcpyDeviceToHost,
                                   (cudaStream_t)stream);

@@ -64,17 +64,17 @@ extern "C" bl_status bl_attn_bwd_noalloc(const bl_shape* shape, const void* q, c
 
   bl::Shape sh;
   if (bl::check_shape(shape, &sh) != BL_OK) return BL_ERR_INVALID_ARG;  // unreachable: need > 0
-  if (sh.strided && !bl::bwd_tc_supported(sh)) return BL_ERR_UNSUPPORTED;
   // Same layout as the workspace of bl_attn_bwd.  The preprocessing kernel
   // that launch_bwd runs first writes every D entry and zeroes the dQ
   // accumulator and the status word, so nothing left by an earlier call leaks
   // into this one.
   float* ws_D = reinterpret_cast<float*>(ws);
   float* ws_dq = reinterpret_cast<float*>(ws + bl::ws_D_bytes(sh));
-  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + bl::ws_D_bytes(sh) + bl::ws_dq_bytes(sh));
+  int32_t* ws_sub = reinterpret_cast<int32_t*>(ws + bl::ws_D_bytes(sh) + bl::ws_dq_bytes(sh));
+  int32_t* ws_status = reinterpret_cast<int32_t*>(ws + bl::ws_status_off(sh));
   cudaError_t e = bl::launch_bwd(sh, q, k, v, o, g_o, lse, scale, lists ? lists->q_idx : nullptr,
                                  lists ? lists->q_cnt : nullptr, g_q, g_k, g_v, ws_D, ws_dq,
-                                 ws_status, (cudaStream_t)stream);
+                                 ws_sub, ws_status, (cudaStream_t)stream);
   return e == cudaSuccess ? BL_OK : BL_ERR_CUDA;
 }
 
@@ -89,7 +89,7 @@ extern "C" bl_status bl_bwd_noalloc_check_status(const bl_shape* shape, void* st
   const unsigned char* ws = static_cast<const unsigned char*>(scratch_address());
   if (!ws) return BL_ERR_CUDA;
   const int32_t* st =
-      reinterpret_cast<const int32_t*>(ws + bl::ws_D_bytes(sh) + bl::ws_dq_bytes(sh));
+      reinterpret_cast<const int32_t*>(ws + bl::ws_status_off(sh));
   int32_t host = 0;
   cudaError_t e = cudaMemcpyAsync(&host, st, sizeof(int32_t), cudaMemcpyDeviceToHost,
                                   (cudaStream_t)stream);

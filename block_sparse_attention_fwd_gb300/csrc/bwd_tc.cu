@@ -1,5 +1,8 @@
-// Block-sparse attention backward on tcgen05 tensor cores (sm_103a), 128 x
-// 128 tiles, head dim 64 or 128.
+// Block-sparse attention backward on tcgen05 tensor cores (sm_103a), head dim
+// 64 or 128.  The products run on 128 x 128 tiles; a mask of 64-wide tiles is
+// regrouped into lists of 128 x 128 tiles whose entries carry which 64 x 64
+// quarters are kept (sub_lists_kernel), and a dropped quarter's P^T is 0, so
+// it adds nothing to any gradient: the same result as skipping it.
 //
 // Math ("Introducing BackLite", Backpropagation for attention; Using
 // Sparsity): for every kept tile pair (query tile i, key tile j)
@@ -65,6 +68,8 @@
 // they add nothing to any gradient; the mask never keeps a tile without an
 // attending pair and, without lists, the walk skips such tiles.
 // All hand-offs are mbarriers; every wait is bounded (tc.cuh).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -139,11 +144,15 @@ __device__ __forceinline__ Item item_of(const Shape& sh, int m) {
 // list buffer when they were cached there, else from global memory.  The
 // pointers are passed to next() (kernel parameters and a shared-memory base)
 // rather than held, so a walk keeps only its counters in registers.
+// With SUB, list entries carry a 64 x 64 sub-tile mask in bits 24-27 (bit
+// 2 * query half + key half set = that quarter of the 128 x 128 tile is kept);
+// the walk returns it in `sub`.  Without SUB every quarter is kept.
+template <bool SUB>
 struct Walk {
   int j, b, hk;
   bool cached;
   int gi = 0, li = 0, cnt = -1;
-  int h = 0, i = 0;
+  int h = 0, i = 0, sub = 15;
   bool corrupt = false;
   __device__ bool next(const Shape& sh, int G, const int32_t* q_idx, const int32_t* q_cnt,
                        const int32_t* s_list, const int32_t* s_cnt, const int32_t* s_base) {
@@ -172,6 +181,10 @@ struct Walk {
         i = s_list[s_base[gi] + li];
       else
         i = q_idx ? q_idx[(bh * sh.T_c + j) * (int64_t)sh.T_r + li] : li;
+      if (SUB) {
+        sub = (i >> 24) & 15;
+        i &= 0xFFFFFF;
+      }
       ++li;
       if (i < 0 || i >= sh.T_r) {
         corrupt = true;
@@ -185,8 +198,10 @@ struct Walk {
 
 __device__ __forceinline__ bool failed(const int* f) { return *(volatile const int*)f != 0; }
 
-// MASKED: causal / sliding-window element masks are compiled in.
-template <int D, bool MASKED>
+// MASKED: causal / sliding-window element masks; SUB: sub-tile lists (64-wide
+// tiles of the mask, computed as 128 x 128 tiles with the dropped quarters'
+// P^T set to 0).
+template <int D, bool MASKED, bool SUB>
 __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -256,14 +271,14 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
   int32_t* s_lbase0 = reinterpret_cast<int32_t*>(sm + C::OFF_LBASE);
   // the walk of an item over list buffer buf (filled by warps 2-3)
   auto make_walk = [&](const Item& it, int buf) {
-    Walk w;
+    Walk<SUB> w;
     w.j = it.j;
     w.b = it.b;
     w.hk = it.hk;
     w.cached = s_cached[buf] != 0;
     return w;
   };
-  auto step = [&](Walk& w, int buf) {
+  auto step = [&](Walk<SUB>& w, int buf) {
     return w.next(sh, G, q_idx, q_cnt, s_list0 + buf * C::LIST_CAP, s_lcnt0 + buf * C::GMAX,
                   s_lbase0 + buf * C::GMAX);
   };
@@ -282,7 +297,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       const int m = s_item[buf];
       if (m < 0) break;
       const Item it = item_of(sh, m);
-      Walk walk = make_walk(it, buf);
+      Walk<SUB> walk = make_walk(it, buf);
       bool first = true;
       while (ok && step(walk, buf)) {
         const int64_t bh = (int64_t)it.b * sh.H + walk.h;
@@ -387,7 +402,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         const int m = s_item[buf];
         if (m < 0) break;
         const Item it = item_of(sh, m);
-        Walk walk = make_walk(it, buf);
+        Walk<SUB> walk = make_walk(it, buf);
         bool have = step(walk, buf);
         if (have) {
           // the item's first tile: S^T needs its K, dP^T its V and a drained R_dP
@@ -549,7 +564,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       const int m = s_item[buf];
       if (m < 0) break;
       const Item it = item_of(sh, m);
-      Walk walk = make_walk(it, buf);
+      Walk<SUB> walk = make_walk(it, buf);
       const int j = it.j;
       const bool key_ok = j * 128 + r < sh.n;
       int nt = 0;
@@ -561,6 +576,8 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
                                          mbar_wait(&bars.s_full, t & 1));
         if (!ok) break;
         fence_after_sync();
+        // a dropped 64 x 64 quarter (SUB) contributes P^T = 0, like a key past n
+        const bool key_on = key_ok && (!SUB || ((walk.sub >> (2 * half + (r >> 6))) & 1));
         const float* sl = reinterpret_cast<const float*>(sm + C::OFF_L) + s * 128 + half * 64;
         const float* sd = reinterpret_cast<const float*>(sm + C::OFF_D) + s * 128 + half * 64;
         // this key row attends query columns q_lo..q_hi of the warpgroup's 64:
@@ -587,7 +604,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
               for (int y = 0; y < 4; ++y) {
                 const int c = 4 * c4 + y;
                 pf[c0 + c] =
-                    key_ok ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
+                    key_on ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
               }
             }
             if (diag) {
@@ -747,7 +764,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       const int m = s_item[buf];
       if (m < 0) break;
       const Item it = item_of(sh, m);
-      Walk walk = make_walk(it, buf);
+      Walk<SUB> walk = make_walk(it, buf);
       while (ok && step(walk, buf)) {
         ok = agree(!failed(&s_fail) && mbar_wait(&bars.dq_ready, u & 1));
         if (!ok) break;
@@ -802,7 +819,7 @@ int sm_count() {
   return count[dev];
 }
 
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool SUB>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, const void* g_o,
                      const float* lse, const float* Dv, const int32_t* q_idx,
                      const int32_t* q_cnt, void* g_k, void* g_v, float* dq_acc, int32_t* status,
@@ -818,7 +835,7 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
       !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
-  auto kern = bwd_tc_kernel<D, MASKED>;
+  auto kern = bwd_tc_kernel<D, MASKED, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)sh.T_c * sh.Hk * sh.B;
@@ -829,26 +846,123 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   return cudaGetLastError();
 }
 
+// Lists of 64-wide tiles as lists of 128 x 128 tiles: for every (batch,
+// head, 128-key tile) the ascending 128-row query tiles that hold a kept
+// 64 x 64 quarter, each entry carrying the quarter mask in bits 24-27 (bit
+// 2 * query half + key half).  A 128-wide side keeps both of its halves
+// together.  Entries and counts out of range are skipped and recorded in the
+// status word, as the walk does.  One CTA of 128 threads per (128-key tile,
+// head, batch); `bits` in dynamic shared memory, one word per 128-row tile.
+__global__ void __launch_bounds__(128) sub_lists_kernel(const int32_t* __restrict__ q_idx,
+                                                        const int32_t* __restrict__ q_cnt,
+                                                        Shape sh, Shape sh128,
+                                                        int32_t* __restrict__ out_idx,
+                                                        int32_t* __restrict__ out_cnt,
+                                                        int32_t* __restrict__ status) {
+  extern __shared__ uint32_t bits[];
+  __shared__ int s_wcnt[4];
+  const int J = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bh = (int64_t)blockIdx.z * sh.H + blockIdx.y;
+  const int R = sh128.T_r;
+  for (int x = tid; x < R; x += 128) bits[x] = 0;
+  __syncthreads();
+  const int nsrc = sh.block_k == 64 ? 2 : 1;
+  bool bad = false;
+  for (int e = 0; e < nsrc; ++e) {
+    const int j = nsrc == 2 ? 2 * J + e : J;
+    if (j >= sh.T_c) break;
+    const uint32_t kmask = sh.block_k == 64 ? (1u << e) : 3u;   // key halves of this tile
+    int cnt = q_cnt[bh * sh.T_c + j];
+    if (cnt < 0 || cnt > sh.T_r) {
+      bad = true;
+      cnt = 0;
+    }
+    const int32_t* list = q_idx + (bh * sh.T_c + j) * (int64_t)sh.T_r;
+    for (int li = tid; li < cnt; li += 128) {
+      const int i = list[li];
+      if (i < 0 || i >= sh.T_r) {
+        bad = true;
+        continue;
+      }
+      const int I = sh.block_q == 64 ? i >> 1 : i;
+      const uint32_t qmask = sh.block_q == 64 ? (1u << (i & 1)) : 3u;   // query halves
+      uint32_t m = 0;
+      for (int qh = 0; qh < 2; ++qh)
+        if (qmask & (1u << qh)) m |= kmask << (2 * qh);
+      atomicOr(&bits[I], m);
+    }
+  }
+  if (bad) atomicOr(status, tc::kStatusCorrupt);
+  __syncthreads();
+  // compact the non-empty 128-row tiles in ascending order
+  int32_t* orow = out_idx + (bh * sh128.T_c + J) * (int64_t)R;
+  int run = 0;
+  for (int x0 = 0; x0 < R; x0 += 128) {
+    const int x = x0 + tid;
+    const uint32_t m = x < R ? bits[x] : 0u;
+    const unsigned bal = __ballot_sync(0xffffffffu, m != 0);
+    if (lane == 0) s_wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int off = run;
+    for (int w = 0; w < warp; ++w) off += s_wcnt[w];
+    if (m) orow[off + __popc(bal & ((1u << lane) - 1u))] = x | (int)(m << 24);
+    run += s_wcnt[0] + s_wcnt[1] + s_wcnt[2] + s_wcnt[3];
+    __syncthreads();
+  }
+  if (tid == 0) out_cnt[bh * sh128.T_c + J] = run;
+}
+
 }  // namespace
 
-bool bwd_tc_supported(const Shape& sh) {
-  return sh.block_q == 128 && sh.block_k == 128 && (sh.d == 64 || sh.d == 128);
+bool bwd_tc_supported(const Shape& sh) { return sh.d == 64 || sh.d == 128; }
+
+// The 128 x 128 view of a shape with 64-wide tiles.
+Shape tiles128(const Shape& sh) {
+  Shape t = sh;
+  t.block_q = t.block_k = 128;
+  t.T_r = t.T_c = (sh.n + 127) / 128;
+  t.n_pad = (int64_t)t.T_r * 128;
+  return t;
+}
+
+size_t bwd_sub_lists_bytes(const Shape& sh) {
+  if (sh.block_q == 128 && sh.block_k == 128) return 0;
+  const Shape t = tiles128(sh);
+  const size_t e = (size_t)sh.B * sh.H * t.T_c * ((size_t)t.T_r + 1);
+  return (e * sizeof(int32_t) + 255) & ~(size_t)255;
 }
 
 cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const void* v,
                           const void* g_o, const float* lse, const float* Dv,
                           const int32_t* q_idx, const int32_t* q_cnt, void* g_k, void* g_v,
-                          float* dq_acc, int32_t* status, float scale, cudaStream_t st) {
+                          float* dq_acc, int32_t* sub_ws, int32_t* status, float scale,
+                          cudaStream_t st) {
   const bool masked = sh.causal || sh.window;
-  if (sh.d == 128)
-    return masked ? launch_t<128, true>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
-                                        status, scale, st)
-                  : launch_t<128, false>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
-                                         status, scale, st);
-  return masked ? launch_t<64, true>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
-                                     status, scale, st)
-                : launch_t<64, false>(sh, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc,
-                                      status, scale, st);
+  const bool sub = !(sh.block_q == 128 && sh.block_k == 128);
+  const Shape s128 = tiles128(sh);
+  if (sub && q_idx) {   // 64-wide tiles: lists of 128 x 128 tiles with quarter masks
+    if ((size_t)s128.T_r * sizeof(uint32_t) > 48 * 1024) return cudaErrorInvalidValue;
+    int32_t* idx = sub_ws;
+    int32_t* cnt = sub_ws + (size_t)sh.B * sh.H * s128.T_c * s128.T_r;
+    dim3 g(s128.T_c, sh.H, sh.B);
+    sub_lists_kernel<<<g, 128, (size_t)s128.T_r * sizeof(uint32_t), st>>>(q_idx, q_cnt, sh, s128,
+                                                                          idx, cnt, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    q_idx = idx;
+    q_cnt = cnt;
+  }
+  auto go = [&](auto d_c, auto m_c, auto s_c) {
+    return launch_t<decltype(d_c)::value, decltype(m_c)::value, decltype(s_c)::value>(
+        s128, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc, status, scale, st);
+  };
+  using I64 = std::integral_constant<int, 64>;
+  using I128 = std::integral_constant<int, 128>;
+  using T = std::true_type;
+  using F = std::false_type;
+  if (sub && q_idx) return sh.d == 128 ? go(I128{}, F{}, T{}) : go(I64{}, F{}, T{});
+  if (sh.d == 128) return masked ? go(I128{}, T{}, F{}) : go(I128{}, F{}, F{});
+  return masked ? go(I64{}, T{}, F{}) : go(I64{}, F{}, F{});
 }
 
 }  // namespace bl

@@ -22,19 +22,23 @@ cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
                         int32_t* nan_count, cudaStream_t st);
 
 // Backward.  q_idx/q_cnt == nullptr runs every tile.  ws_D [B,H,n] fp32,
-// ws_dq [B,n,H,d] fp32, ws_status one int32.
+// ws_dq [B,n,H,d] fp32, ws_sub bwd_sub_lists_bytes(sh) (64-wide tiles),
+// ws_status two int32.
 cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void* v,
                        const void* o, const void* g_o, const float* lse, float scale,
                        const int32_t* q_idx, const int32_t* q_cnt, void* g_q, void* g_k,
-                       void* g_v, float* ws_D, float* ws_dq, int32_t* ws_status,
-                       cudaStream_t st);
+                       void* g_v, float* ws_D, float* ws_dq, int32_t* ws_sub,
+                       int32_t* ws_status, cudaStream_t st);
 
-// tcgen05 dK/dV/dQ pass for 128 x 128 tiles (head dim 64 or 128).
+// tcgen05 dK/dV/dQ pass (head dim 64 or 128).  Shapes with 64-wide tiles run
+// as 128 x 128 tiles whose lists (built in sub_ws) carry 64 x 64 quarter masks.
 bool bwd_tc_supported(const Shape& sh);
+size_t bwd_sub_lists_bytes(const Shape& sh);
 cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const void* v,
                           const void* g_o, const float* lse, const float* Dv,
                           const int32_t* q_idx, const int32_t* q_cnt, void* g_k, void* g_v,
-                          float* dq_acc, int32_t* status, float scale, cudaStream_t st);
+                          float* dq_acc, int32_t* sub_ws, int32_t* status, float scale,
+                          cudaStream_t st);
 
 // tcgen05 forward with tile statistics for 128 x 128 tiles (head dim 64 or
 // 128).  logw != nullptr also writes the tile weights [B,H,T_r,T_c]; with

@@ -114,7 +114,7 @@ bl_status make_plan(const bl_varlen* v, Plan* p) {
     z.q_idx += BH * r.sh.T_c * r.sh.T_r;
     z.q_cnt += BH * r.sh.T_c;
     r.ws = p->ws_areas;
-    p->ws_areas += bl::ws_D_bytes(r.sh) + bl::ws_dq_bytes(r.sh);
+    p->ws_areas += bl::ws_D_bytes(r.sh) + bl::ws_dq_bytes(r.sh) + bl::ws_sub_bytes(r.sh);
     r.work = r.sh.B * (double)r.sh.H * attending_tiles(r.sh);
     p->runs.push_back(r);
     s = e;
@@ -284,13 +284,15 @@ bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void*
   return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
     float* ws_D = reinterpret_cast<float*>(ws + r.ws);
     float* ws_dq = reinterpret_cast<float*>(ws + r.ws + bl::ws_D_bytes(r.sh));
+    int32_t* ws_sub =
+        reinterpret_cast<int32_t*>(ws + r.ws + bl::ws_D_bytes(r.sh) + bl::ws_dq_bytes(r.sh));
     const size_t idx = (size_t)(&r - p.runs.data());
     return bl::launch_bwd(
         r.sh, rows(q, r.tok, H, d), rows(k, r.tok, Hk, d), rows(v, r.tok, Hk, d),
         rows(o, r.tok, H, d), rows(g_o, r.tok, H, d), lse + r.lse, scale,
         lists ? lists->q_idx + r.q_idx : nullptr, lists ? lists->q_cnt + r.q_cnt : nullptr,
         rows(g_q, r.tok, H, d), rows(g_k, r.tok, Hk, d), rows(g_v, r.tok, Hk, d), ws_D, ws_dq,
-        status_slot(workspace, p, idx), st);
+        ws_sub, status_slot(workspace, p, idx), st);
   });
 }
 

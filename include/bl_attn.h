@@ -73,8 +73,8 @@ typedef struct {
    * v_strides for v and g_v, o_strides for o and g_o.  All four entries 0
    * (what a zero-initialised struct holds) means contiguous BSHD.  Otherwise
    * the dim stride is 1, the others positive multiples of 8 (16 bytes), and
-   * the head stride at least d.  Strided tensors need the tcgen05 backward
-   * (128 x 128 tiles); the packed (varlen) calls take contiguous tensors. */
+   * the head stride at least d.  The packed (varlen) calls take contiguous
+   * tensors. */
   int64_t q_strides[4], k_strides[4], v_strides[4], o_strides[4];
 } bl_shape;
 
@@ -110,8 +110,9 @@ size_t bl_tile_stats_elems(const bl_shape* shape);
 size_t bl_lists_elems(const bl_shape* shape, size_t out[5]);
 
 /* Bytes of device workspace bl_attn_bwd needs (16-byte aligned base):
- * D = rowsum(G_O * O) [B,H,n] fp32, the fp32 dQ accumulator [B,n,H,d], a
- * device status word and the backward kernel's work-item counter.  The call
+ * D = rowsum(G_O * O) [B,H,n] fp32, the fp32 dQ accumulator [B,n,H,d], with
+ * 64-wide tiles the tile lists regrouped into 128 x 128 tiles, a device
+ * status word and the backward kernel's work-item counter.  The call
  * initialises all of it, so the workspace needs no clearing between calls;
  * two calls in flight at the same time must not share one. */
 size_t bl_bwd_workspace_bytes(const bl_shape* shape);

@@ -176,7 +176,14 @@ def test_varlen_layout_matches_the_oracle_layout(lib, cu, bq, bk):
             runs[-1][0] += 1
         else:
             runs.append([1, n])
-    want = sum(-(-(b * 4 * n * 4) // 256) * 256 + b * n * 4 * 64 * 4 for b, n in runs)
+    def sub(b, n):   # 64-wide tiles: lists regrouped into 128 x 128 tiles (+ counts)
+        if bq == 128 and bk == 128:
+            return 0
+        t = -(-n // 128)
+        return -(-(b * 4 * t * (t + 1) * 4) // 256) * 256
+
+    want = sum(-(-(b * 4 * n * 4) // 256) * 256 + b * n * 4 * 64 * 4 + sub(b, n)
+               for b, n in runs)
     assert sz.bwd_workspace_bytes == want + 16 * len(runs)
 
 
@@ -320,8 +327,10 @@ def test_varlen_splits_runs_longer_than_the_grid_limit(lib):
     assert sz.groups == 2
     assert (sz.total, sz.lse, sz.tile_stats, sz.mask, sz.kv_cnt) == \
         (70000, 2 * 70000, 2 * 64 * 70000, 2 * 70000, 2 * 70000)
-    # one D area (256-byte rounded) and one dQ area per group, one 16-byte slot each
-    want = sum(-(-(b * 2 * 4) // 256) * 256 + b * 2 * 64 * 4 for b in (65535, 4465)) + 2 * 16
+    # one D area (256-byte rounded), one dQ area and (64-wide tiles) one area of
+    # regrouped lists per group, one 16-byte slot each
+    want = sum(-(-(b * 2 * 4) // 256) * 256 + b * 2 * 64 * 4 + -(-(b * 2 * 1 * 2 * 4) // 256) * 256
+               for b in (65535, 4465)) + 2 * 16
     assert sz.bwd_workspace_bytes == want
 
 
@@ -373,8 +382,7 @@ def test_varlen_layout_matches_the_oracle_on_random_batches(lib):
 
 def test_strided_shapes_are_validated_on_the_host(lib):
     """bl_shape strides: zero means contiguous; otherwise the dim stride is 1,
-    the others positive multiples of 8 elements, the head stride at least d.
-    A strided backward needs 128 x 128 tiles (host check before any launch)."""
+    the others positive multiples of 8 elements, the head stride at least d."""
     from block_sparse_attention_fwd_gb300 import _lib
     base = _lib.make_shape(1, 1000, 4, 2, 64, 128, 128)
     want = _lib.tile_stats_elems(base)
@@ -392,10 +400,3 @@ def test_strided_shapes_are_validated_on_the_host(lib):
                 (1000 * 16 * 64, 16 * 64, 32, 1),      # heads overlap
                 (0, 16 * 64, 64, 1)):                  # non-positive
         assert _lib.tile_stats_elems(with_q(bad)) == 0
-    s64 = _lib.make_shape(1, 1000, 4, 2, 64, 64, 64)
-    for i, x in enumerate((1000 * 16 * 64, 16 * 64, 64, 1)):
-        s64.q_strides[i] = x
-    ok = ctypes.c_void_p(0x10000)
-    r = lib.bl_attn_bwd(ctypes.byref(s64), ok, ok, ok, ok, ok, ok, 0.125, None, ok, ok, ok, ok,
-                        1 << 30, None)
-    assert r == 2                                   # BL_ERR_UNSUPPORTED
