@@ -24,7 +24,7 @@ EXPORTS = ("bl_tile_stats_elems", "bl_lists_elems", "bl_bwd_workspace_bytes", "b
            "bl_mask_from_tile_weights", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
            "bl_attn_bwd_noalloc", "bl_bwd_noalloc_check_status", "bl_lse_combine", "bl_grad_error", "bl_varlen_layout",
            "bl_attn_fwd_varlen", "bl_mask_from_stats_varlen", "bl_attn_bwd_varlen",
-           "bl_varlen_bwd_check_status")
+           "bl_varlen_bwd_check_status", "bl_set_wait_limit")
 
 
 class Shape(ctypes.Structure):
@@ -122,6 +122,8 @@ def load():
     lib.bl_attn_bwd_varlen.restype = ctypes.c_int
     lib.bl_varlen_bwd_check_status.argtypes = [V, P, P]
     lib.bl_varlen_bwd_check_status.restype = ctypes.c_int
+    lib.bl_set_wait_limit.argtypes = [D]
+    lib.bl_set_wait_limit.restype = D
     lib.bl_status_string.argtypes = [ctypes.c_int]
     lib.bl_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -344,6 +346,12 @@ def attn_bwd_noalloc(shape, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v):
                                       ctypes.byref(ls) if ls is not None else None,
                                       _ptr(g_q), _ptr(g_k), _ptr(g_v), _stream(q.device))
     _check("bl_attn_bwd_noalloc", code)
+
+
+def set_wait_limit(seconds: float) -> float:
+    """bl_set_wait_limit: the device-side wait limit for later launches (seconds
+    in [0, 2); anything else restores 2 s).  Returns the previous limit."""
+    return float(load().bl_set_wait_limit(float(seconds)))
 
 
 def bwd_noalloc_check_status(shape, device=None) -> int:

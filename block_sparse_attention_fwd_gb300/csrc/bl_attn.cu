@@ -3,12 +3,21 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/bl_attn.h"
 #include "abi.h"
 #include "common.cuh"
 #include "kernels.h"
 
 namespace bl {
+
+namespace {
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 bl_status check_shape(const bl_shape* s, Shape* out) {
   if (!s) return BL_ERR_INVALID_ARG;
@@ -227,6 +236,12 @@ bl_status bl_grad_error(const void* a, const void* b, size_t n, double* out, voi
   if (!aligned16(a) || !aligned16(b) || (reinterpret_cast<uintptr_t>(out) & 7u))
     return BL_ERR_INVALID_ARG;
   return cuda_status(bl::launch_grad_error(a, b, (int64_t)n, out, (cudaStream_t)stream));
+}
+
+double bl_set_wait_limit(double seconds) {
+  uint64_t v = bl::kDefaultWaitNs;
+  if (seconds >= 0.0 && seconds < 2.0) v = (uint64_t)(seconds * 1e9);
+  return (double)bl::g_wait_ns.exchange(v) * 1e-9;
 }
 
 const char* bl_status_string(bl_status status) {

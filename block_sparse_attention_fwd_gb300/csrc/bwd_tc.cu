@@ -115,6 +115,7 @@ constexpr int kListUsers = 14;
 struct Bars {
   uint64_t kv_full, kv_empty, full[3], empty[3], s_full, dp_full, p1_ready, p2_ready;
   uint64_t dq_ready, dq_free, acc_full, list_full[2], list_empty[2];
+  uint64_t quiesce;   // the MMA issuer's last commit, waited for before TMEM is freed
 };
 
 // Load x = 2t brings Q_t, x = 2t + 1 brings dO_t.  Q_t alternates between
@@ -201,7 +202,8 @@ __device__ __forceinline__ bool failed(const int* f) { return *(volatile const i
 // MASKED: causal / sliding-window element masks; SUB: sub-tile lists (64-wide
 // tiles of the mask, computed as 128 x 128 tiles with the dropped quarters'
 // P^T set to 0).
-template <int D, bool MASKED, bool SUB>
+// WL: the launch runs under a non-default wait limit (bl_set_wait_limit).
+template <int D, bool MASKED, bool SUB, bool WL>
 __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const float* __restrict__ Dv, const int32_t* __restrict__ q_idx,
     const int32_t* __restrict__ q_cnt, __nv_bfloat16* __restrict__ g_k,
     __nv_bfloat16* __restrict__ g_v, int32_t* __restrict__ status, Shape sh, float scale,
-    float scale_log2) {
+    float scale_log2, uint64_t wait_ns) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -218,6 +220,9 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
+  __shared__ uint64_t s_wait;      // the launch's wait limit (ns)
+  // parity of the last load armed on full[0..2] and on kv_full (-1: none)
+  __shared__ int s_par[4];
   __shared__ int s_cached[2];
   __shared__ int s_item[2];        // item of each list buffer, -1: no more items
   __shared__ int s_drain_ok[4];
@@ -242,11 +247,14 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     mbar_init(&bars.dq_ready, 1);
     mbar_init(&bars.dq_free, 128);
     mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.quiesce, 1);
     for (int u = 0; u < 2; ++u) {
       mbar_init(&bars.list_full[u], 64);
       mbar_init(&bars.list_empty[u], kListUsers);
     }
     s_fail = 0;
+    s_wait = wait_ns;
+    s_par[0] = s_par[1] = s_par[2] = s_par[3] = -1;
     fence_mbar_init();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -261,6 +269,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
+
 
   auto fail = [&]() {
     atomicOr(&s_fail, 1);
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int buf = k & 1;
-      ok = !failed(&s_fail) && mbar_wait(&bars.list_full[buf], (k >> 1) & 1);
+      ok = !failed(&s_fail) && wait_phase<WL>(&bars.list_full[buf], (k >> 1) & 1, &s_wait);
       if (!ok) break;
       const int m = s_item[buf];
       if (m < 0) break;
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
               dv[e] = in ? Dv[bh * sh.n + r] : 0.f;
             }
           }
-          ok = !failed(&s_fail) && mbar_wait(&bars.empty[s], phase_of(x) ^ 1);
+          ok = !failed(&s_fail) && wait_phase<WL>(&bars.empty[s], phase_of(x) ^ 1, &s_wait);
           if (!ok) break;
           if (lane == 0) {
             mbar_expect_tx(&bars.full[s], C::TILE);
@@ -332,9 +341,10 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             }
           }
           mbar_arrive(&bars.full[s]);
+          if (lane == 0) s_par[s] = (int)phase_of(x);
           if (which == 0 && first) {
             // this item's K_j and V_j, once the previous item's last dQ has read K
-            ok = mbar_wait(&bars.kv_empty, (kk & 1) ^ 1);
+            ok = wait_phase<WL>(&bars.kv_empty, (kk & 1) ^ 1, &s_wait);
             if (!ok) break;
             if (lane == 0) {
               mbar_expect_tx(&bars.kv_full, 2 * C::TILE);
@@ -345,6 +355,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
                             it.j * 128, it.b);
               }
             }
+            if (lane == 0) s_par[3] = kk & 1;
             first = false;
           }
         }
@@ -390,14 +401,14 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         mma_commit(&bars.dp_full);
       };
       auto wait_slot = [&](int xx) {
-        return mbar_wait(&bars.full[slot_of(xx)], phase_of(xx));
+        return wait_phase<WL>(&bars.full[slot_of(xx)], phase_of(xx), &s_wait);
       };
       int t = 0;     // tile index over all items
       int kk = 0;    // items with at least one tile so far
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int buf = k & 1;
-        ok = !failed(&s_fail) && mbar_wait(&bars.list_full[buf], (k >> 1) & 1);
+        ok = !failed(&s_fail) && wait_phase<WL>(&bars.list_full[buf], (k >> 1) & 1, &s_wait);
         if (!ok) break;
         const int m = s_item[buf];
         if (m < 0) break;
@@ -406,11 +417,11 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         bool have = step(walk, buf);
         if (have) {
           // the item's first tile: S^T needs its K, dP^T its V and a drained R_dP
-          ok = mbar_wait(&bars.kv_full, kk & 1) && wait_slot(2 * t);
+          ok = wait_phase<WL>(&bars.kv_full, kk & 1, &s_wait) && wait_slot(2 * t);
           if (!ok) break;
           fence_after_sync();
           issue_s(t);
-          ok = (t == 0 || mbar_wait(&bars.dq_free, (t - 1) & 1)) && wait_slot(2 * t + 1);
+          ok = (t == 0 || wait_phase<WL>(&bars.dq_free, (t - 1) & 1, &s_wait)) && wait_slot(2 * t + 1);
           if (!ok) break;
           fence_after_sync();
           issue_dp(t);
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         while (ok && have) {
           // dV_t as soon as the first softmax phase has written P^T; it runs
           // while the second phase forms dS^T
-          ok = !failed(&s_fail) && mbar_wait(&bars.p1_ready, t & 1);
+          ok = !failed(&s_fail) && wait_phase<WL>(&bars.p1_ready, t & 1, &s_wait);
           if (!ok) break;
           fence_after_sync();
           const uint64_t gmn = sdesc_sw128(slot_addr(2 * t + 1), C::CHUNK, 1024);
@@ -440,7 +451,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             issue_s(t + 1);
           }
           // dK_t once dS^T is in shared memory
-          ok = mbar_wait(&bars.p2_ready, t & 1);
+          ok = wait_phase<WL>(&bars.p2_ready, t & 1, &s_wait);
           if (!ok) break;
           fence_after_sync();
           const uint32_t dsb = opaque(sDS);
@@ -465,7 +476,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
           if (next) {
             // dP^T of the next tile once the dQ tile has left R_dP; the dS^T
             // buffer is rewritten only after dP^T completes, hence after dQ
-            ok = mbar_wait(&bars.dq_free, t & 1) && wait_slot(2 * (t + 1) + 1);
+            ok = wait_phase<WL>(&bars.dq_free, t & 1, &s_wait) && wait_slot(2 * (t + 1) + 1);
             if (!ok) break;
             fence_after_sync();
             issue_dp(t + 1);
@@ -498,7 +509,8 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int buf = k & 1;
-      ok = agree(!failed(&s_fail) && mbar_wait(&bars.list_empty[buf], ((k >> 1) & 1) ^ 1));
+      ok = agree(!failed(&s_fail) &&
+                 wait_phase<WL>(&bars.list_empty[buf], ((k >> 1) & 1) ^ 1, &s_wait));
       if (!ok) break;
       if (tt == 0) {
         const int mm = atomicAdd(item_counter, 1);
@@ -559,7 +571,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     for (int k = 0; ok; ++k) {
       const int buf = k & 1;
       ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
-                                       mbar_wait(&bars.list_full[buf], (k >> 1) & 1));
+                                       wait_phase<WL>(&bars.list_full[buf], (k >> 1) & 1, &s_wait));
       if (!ok) break;
       const int m = s_item[buf];
       if (m < 0) break;
@@ -572,8 +584,8 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         const int s = t & 1;                      // Q_t's slot: its LSE and D rows
         // phase 1: P^T from S^T (needs only S^T), written back over S^T
         ok = __all_sync(0xffffffffu, !failed(&s_fail) &&
-                                         mbar_wait(&bars.full[s], (t >> 1) & 1) &&
-                                         mbar_wait(&bars.s_full, t & 1));
+                                         wait_phase<WL>(&bars.full[s], (t >> 1) & 1, &s_wait) &&
+                                         wait_phase<WL>(&bars.s_full, t & 1, &s_wait));
         if (!ok) break;
         fence_after_sync();
         // a dropped 64 x 64 quarter (SUB) contributes P^T = 0, like a key past n
@@ -623,7 +635,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         fence_before_sync();
         mbar_arrive(&bars.p1_ready);               // dV_t may read P^T now
         // phase 2: dS^T = P^T (dP^T - D) once dP^T has landed
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, t & 1));
+        ok = __all_sync(0xffffffffu, wait_phase<WL>(&bars.dp_full, t & 1, &s_wait));
         if (!ok) break;
         fence_after_sync();
         if (store_pending) {                       // the rows are about to be overwritten
@@ -681,8 +693,8 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       // stores to have read it only before it next writes dS^T there.
       const Item ie = item_of(sh, s_item[buf]);
       if (nt > 0) {
-        ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.acc_full, kk & 1) &&
-                                         mbar_wait(&bars.dq_ready, (t - 1) & 1));
+        ok = __all_sync(0xffffffffu, !failed(&s_fail) && wait_phase<WL>(&bars.acc_full, kk & 1, &s_wait) &&
+                                         wait_phase<WL>(&bars.dq_ready, (t - 1) & 1, &s_wait));
         if (!ok) break;
         fence_after_sync();
         ++kk;
@@ -759,14 +771,14 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int buf = k & 1;
-      ok = agree(!failed(&s_fail) && mbar_wait(&bars.list_full[buf], (k >> 1) & 1));
+      ok = agree(!failed(&s_fail) && wait_phase<WL>(&bars.list_full[buf], (k >> 1) & 1, &s_wait));
       if (!ok) break;
       const int m = s_item[buf];
       if (m < 0) break;
       const Item it = item_of(sh, m);
       Walk<SUB> walk = make_walk(it, buf);
       while (ok && step(walk, buf)) {
-        ok = agree(!failed(&s_fail) && mbar_wait(&bars.dq_ready, u & 1));
+        ok = agree(!failed(&s_fail) && wait_phase<WL>(&bars.dq_ready, u & 1, &s_wait));
         if (!ok) break;
         fence_after_sync();
         uint32_t a[D];
@@ -803,6 +815,26 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
 
   fence_before_sync();
   __syncthreads();
+  if (failed(&s_fail)) {
+    // A role gave up on a wait, so loads and MMAs it meant to consume may still
+    // be in flight: the producer waits for the last load of every barrier it
+    // armed (its phase parity recorded in s_par as it was issued), the MMA
+    // issuer for a commit behind its last MMA, before the tensor memory is
+    // freed and the CTA exits.  (Without a failure every load and MMA has been
+    // consumed by then.)
+    if (warp == 0 && lane == 0) {
+#pragma unroll
+      for (int sl = 0; sl < 3; ++sl)
+        if (s_par[sl] >= 0) mbar_wait_poll(&bars.full[sl], (uint32_t)s_par[sl]);
+      if (s_par[3] >= 0) mbar_wait_poll(&bars.kv_full, (uint32_t)s_par[3]);
+    }
+    if (warp == 1 && lane == 0) {
+      mma_commit(&bars.quiesce);
+      mbar_wait_poll(&bars.quiesce, 0);
+    }
+    fence_before_sync();
+    __syncthreads();
+  }
   if (warp == 1) tmem_free(tmem, C::T_COLS);
 }
 
@@ -819,7 +851,7 @@ int sm_count() {
   return count[dev];
 }
 
-template <int D, bool MASKED, bool SUB>
+template <int D, bool MASKED, bool SUB, bool WL>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, const void* g_o,
                      const float* lse, const float* Dv, const int32_t* q_idx,
                      const int32_t* q_cnt, void* g_k, void* g_v, float* dq_acc, int32_t* status,
@@ -835,14 +867,14 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
       !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
-  auto kern = bwd_tc_kernel<D, MASKED, SUB>;
+  auto kern = bwd_tc_kernel<D, MASKED, SUB, WL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)sh.T_c * sh.Hk * sh.B;
   const int grid = (int)(items < sm_count() ? items : sm_count());
   kern<<<grid, 512, smem, st>>>(mq, mk, mv, mg, md, mgk, mgv, lse, Dv, q_idx, q_cnt,
-                                (__nv_bfloat16*)g_k,
-                                (__nv_bfloat16*)g_v, status, sh, scale, scale * kLog2e);
+                                (__nv_bfloat16*)g_k, (__nv_bfloat16*)g_v, status, sh, scale,
+                                scale * kLog2e, wait_limit_ns());
   return cudaGetLastError();
 }
 
@@ -952,17 +984,21 @@ cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const v
     q_idx = idx;
     q_cnt = cnt;
   }
-  auto go = [&](auto d_c, auto m_c, auto s_c) {
-    return launch_t<decltype(d_c)::value, decltype(m_c)::value, decltype(s_c)::value>(
-        s128, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v, dq_acc, status, scale, st);
+  auto run = [&](auto wl_c) {
+    auto go = [&](auto d_c, auto m_c, auto s_c) {
+      return launch_t<decltype(d_c)::value, decltype(m_c)::value, decltype(s_c)::value,
+                      decltype(wl_c)::value>(s128, q, k, v, g_o, lse, Dv, q_idx, q_cnt, g_k, g_v,
+                                             dq_acc, status, scale, st);
+    };
+    using I64 = std::integral_constant<int, 64>;
+    using I128 = std::integral_constant<int, 128>;
+    using T = std::true_type;
+    using F = std::false_type;
+    if (sub && q_idx) return sh.d == 128 ? go(I128{}, F{}, T{}) : go(I64{}, F{}, T{});
+    if (sh.d == 128) return masked ? go(I128{}, T{}, F{}) : go(I128{}, F{}, F{});
+    return masked ? go(I64{}, T{}, F{}) : go(I64{}, F{}, F{});
   };
-  using I64 = std::integral_constant<int, 64>;
-  using I128 = std::integral_constant<int, 128>;
-  using T = std::true_type;
-  using F = std::false_type;
-  if (sub && q_idx) return sh.d == 128 ? go(I128{}, F{}, T{}) : go(I64{}, F{}, T{});
-  if (sh.d == 128) return masked ? go(I128{}, T{}, F{}) : go(I128{}, F{}, F{});
-  return masked ? go(I64{}, T{}, F{}) : go(I64{}, F{}, F{});
+  return wait_limit_ns() != kWaitLimitNs ? run(std::true_type{}) : run(std::false_type{});
 }
 
 }  // namespace bl

@@ -34,6 +34,8 @@
 // the statistics of the key tiles outside [lo, hi] are written as -inf.  The
 // heaviest pairs (latest query tiles) are launched first.
 // Every mbarrier wait is bounded (tc.cuh).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -91,12 +93,13 @@ struct RowScratch {
 
 // SUB: statistics per 128-key MMA tile (1 for 128-key tiles, 2 for 64-key
 // tiles, whose two halves of the S row are summed separately).
-template <int D, int SUB>
+// WL: the launch runs under a non-default wait limit (bl_set_wait_limit).
+template <int D, int SUB, bool WL>
 __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o,
     float* __restrict__ lse, float* __restrict__ stats, float* __restrict__ logw,
-    RowScratch scr, Shape sh, float scale_log2) {
+    RowScratch scr, Shape sh, float scale_log2, uint64_t wait_ns) {
   using C = FCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -104,6 +107,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   __shared__ __align__(8) FBars bars;
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
+  __shared__ uint64_t s_wait;      // the launch's wait limit (ns)
+  __shared__ int s_loads[2];       // K and V visits whose loads the producer issued
   __shared__ int s_slot;
   __shared__ __align__(16) float s_lse[256];   // the pair's final LSE rows (tile weights)
   __shared__ __align__(8) uint64_t s_wbar[2];   // statistics staging buffers (tile weights)
@@ -145,6 +150,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     mbar_init(&s_wbar[0], 1);
     mbar_init(&s_wbar[1], 1);
     s_fail = 0;
+    s_wait = wait_ns;
+    s_loads[0] = s_loads[1] = 0;
     // without a statistics output the rows go to a scratch slot of this CTA's
     // own (claimed from a lock word; at most nslots CTAs are resident at once)
     s_slot = -1;
@@ -170,6 +177,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = s_tmem;
+
   auto fail = [&]() { atomicOr(&s_fail, 1); };
 
   if (warp == 0) {
@@ -186,29 +194,37 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       auto load_v = [&](int jv) -> bool {   // jv counts visits
         const int sv = jv % C::NV;
         // V_(jv-2), the slot's previous tile, is free once done for u = jv - 1
-        if (jv >= C::NV && !mbar_wait(&bars.done[(jv - 1) % 3], ((jv - 1) / 3) & 1)) return false;
+        if (jv >= C::NV && !wait_phase<WL>(&bars.done[(jv - 1) % 3], ((jv - 1) / 3) & 1, &s_wait))
+          return false;
         mbar_expect_tx(&bars.v_full[sv], C::TILE_BYTES);
         for (int c = 0; c < C::CHK; ++c)
           tma_load_4d(sm + C::OFF_V + sv * C::TILE_BYTES + c * C::CHUNK, &tm_v, &bars.v_full[sv],
                       c * 64, hk, (j_lo + jv) * 128, b);
         return true;
       };
+      int k_loads = 0, v_loads = 0;   // visits whose K / V load was issued
       bool ok = true;
       for (int jj = 0; ok && jj <= nj; ++jj) {
         if (jj < nj) {
           const int sk = jj % C::NK;
           // K_(jj-3), the slot's previous tile, is free once done for u = jj - 3
           ok = !failed(&s_fail) &&
-               (jj < C::NK || mbar_wait(&bars.done[sk], ((jj - C::NK) / 3) & 1));
+               (jj < C::NK || wait_phase<WL>(&bars.done[sk], ((jj - C::NK) / 3) & 1, &s_wait));
           if (!ok) break;
           mbar_expect_tx(&bars.k_full[sk], C::TILE_BYTES);
           for (int c = 0; c < C::CHK; ++c)
             tma_load_4d(sm + C::OFF_K + sk * C::TILE_BYTES + c * C::CHUNK, &tm_k,
                         &bars.k_full[sk], c * 64, hk, (j_lo + jj) * 128, b);
+          k_loads = jj + 1;
         }
-        if (jj >= 1) ok = load_v(jj - 1);   // V stays one key tile behind K
+        if (jj >= 1) {                       // V stays one key tile behind K
+          ok = load_v(jj - 1);
+          if (ok) v_loads = jj;
+        }
       }
       if (!ok) fail();
+      s_loads[0] = k_loads;
+      s_loads[1] = v_loads;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -233,7 +249,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
                  sdesc_sw128(vb + kk * 2048, C::CHUNK, 1024), C::ID_O,
                  (jj > 0 || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(&bars.q, 0) && mbar_wait(&bars.k_full[0], 0);
+      bool ok = wait_phase<WL>(&bars.q, 0, &s_wait) && wait_phase<WL>(&bars.k_full[0], 0, &s_wait);
       if (ok) {
         fence_after_sync();
         for (int t = 0; t < ntile; ++t) issue_s(t, 0);
@@ -249,10 +265,10 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
             mbar_test3(saddr(&bars.k_full[(jj + 1) % C::NK]), kp,
                        saddr(&bars.v_full[jj % C::NV]), vp, saddr(&bars.p_ready[0]), jj & 1);
         if (more && !(rd & 1))
-          ok = !failed(&s_fail) && mbar_wait(&bars.k_full[(jj + 1) % C::NK], kp);
-        if (ok && !(rd & 2)) ok = mbar_wait(&bars.v_full[jj % C::NV], vp);
+          ok = !failed(&s_fail) && wait_phase<WL>(&bars.k_full[(jj + 1) % C::NK], kp, &s_wait);
+        if (ok && !(rd & 2)) ok = wait_phase<WL>(&bars.v_full[jj % C::NV], vp, &s_wait);
         for (int t = 0; ok && t < ntile; ++t) {
-          ok = (t == 0 && (rd & 4)) || mbar_wait(&bars.p_ready[t], jj & 1);
+          ok = (t == 0 && (rd & 4)) || wait_phase<WL>(&bars.p_ready[t], jj & 1, &s_wait);
           if (!ok) break;
           fence_after_sync();
           issue_pv(t, jj);
@@ -291,7 +307,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     bool ok = valid_tile;
     for (int jj = 0; ok && jj < nj; ++jj) {
       const int j = j_lo + jj;
-      ok = __all_sync(0xffffffffu, !failed(&s_fail) && mbar_wait(&bars.s_full[t], jj & 1));
+      ok = __all_sync(0xffffffffu,
+                      !failed(&s_fail) && wait_phase<WL>(&bars.s_full[t], jj & 1, &s_wait));
       if (!ok) break;
       fence_after_sync();
       uint32_t x[128];
@@ -432,7 +449,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     }
     if (valid_tile) {
       // epilogue: O = acc / l, LSE = ln 2 (m + log2 l), once the last PV landed
-      const bool done = __all_sync(0xffffffffu, ok && mbar_wait(&bars.o_done[t], 0));
+      const bool done = __all_sync(0xffffffffu, ok && wait_phase<WL>(&bars.o_done[t], 0, &s_wait));
       fence_after_sync();
       const float inv = 1.f / l_run;
       __nv_bfloat16* orow = o + bshd(sh.os, b, row, h);
@@ -517,6 +534,23 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
 
   fence_before_sync();
   __syncthreads();
+  if (failed(&s_fail)) {
+    // A role gave up on a wait, so loads and MMAs it meant to consume may still
+    // be in flight: the producer waits for the last load of every barrier it
+    // armed, the MMA issuer for the commit behind its last MMA, before the
+    // tensor memory is freed and the CTA exits.  (Without a failure every
+    // load and MMA has been consumed by then.)
+    if (warp == 0 && lane == 0) {
+      mbar_wait_poll(&bars.q, 0);
+      for (int u = s_loads[0] - 1; u >= 0 && u >= s_loads[0] - C::NK; --u)
+        mbar_wait_poll(&bars.k_full[u % C::NK], (u / C::NK) & 1);
+      for (int u = s_loads[1] - 1; u >= 0 && u >= s_loads[1] - C::NV; --u)
+        mbar_wait_poll(&bars.v_full[u % C::NV], (u / C::NV) & 1);
+    }
+    if (warp == 1 && lane == 0) mbar_wait_poll(&bars.o_done[0], 0);
+    fence_before_sync();
+    __syncthreads();
+  }
   if (warp == 1) tmem_free(tmem, C::T_COLS);
   if (threadIdx.x == 0 && s_slot >= 0) {   // the slot's rows have all been read
     __threadfence();
@@ -524,7 +558,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
   }
 }
 
-template <int D, int SUB>
+template <int D, int SUB, bool WL>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                      float* lse, float* stats, float* logw, RowScratch scr, float scale,
                      cudaStream_t st) {
@@ -535,7 +569,7 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
       !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128, sh.vs))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
-  auto kern = fwd_tc_kernel<D, SUB>;
+  auto kern = fwd_tc_kernel<D, SUB, WL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (scr.locks) {
@@ -544,7 +578,7 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   }
   dim3 grid(((sh.n + 127) / 128 + 1) / 2, sh.H, sh.B);
   kern<<<grid, 384, smem, st>>>(mq, mk, mv, (__nv_bfloat16*)o, lse, stats, logw, scr, sh,
-                                scale * kLog2e);
+                                scale * kLog2e, wait_limit_ns());
   return cudaGetLastError();
 }
 
@@ -553,7 +587,7 @@ template <int D>
 int resident_ctas() {
   using C = FCfg<D>;
   const int smem = C::BYTES + 1024;
-  auto kern = fwd_tc_kernel<D, 1>;
+  auto kern = fwd_tc_kernel<D, 1, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
@@ -596,13 +630,23 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
     scr.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + locks);
     scr.nslots = ns;
   }
-  if (sh.block_k == 64) {
-    if (logw) return cudaErrorInvalidValue;   // tile weights need 128 x 128 tiles
-    if (sh.d == 128) return launch_t<128, 2>(sh, q, k, v, o, lse, stats, nullptr, scr, scale, st);
-    return launch_t<64, 2>(sh, q, k, v, o, lse, stats, nullptr, scr, scale, st);
+  if (sh.block_k == 64 && logw) return cudaErrorInvalidValue;   // tile weights: 128 x 128 tiles
+  auto go = [&](auto d_c, auto sub_c, auto wl_c) {
+    return launch_t<decltype(d_c)::value, decltype(sub_c)::value, decltype(wl_c)::value>(
+        sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+  };
+  using I64 = std::integral_constant<int, 64>;
+  using I128 = std::integral_constant<int, 128>;
+  using S1 = std::integral_constant<int, 1>;
+  using S2 = std::integral_constant<int, 2>;
+  if (wait_limit_ns() != tc::kWaitLimitNs) {
+    using W = std::true_type;
+    if (sh.block_k == 64) return sh.d == 128 ? go(I128{}, S2{}, W{}) : go(I64{}, S2{}, W{});
+    return sh.d == 128 ? go(I128{}, S1{}, W{}) : go(I64{}, S1{}, W{});
   }
-  if (sh.d == 128) return launch_t<128, 1>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
-  return launch_t<64, 1>(sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+  using N = std::false_type;
+  if (sh.block_k == 64) return sh.d == 128 ? go(I128{}, S2{}, N{}) : go(I64{}, S2{}, N{});
+  return sh.d == 128 ? go(I128{}, S1{}, N{}) : go(I64{}, S1{}, N{});
 }
 
 cudaError_t launch_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o,

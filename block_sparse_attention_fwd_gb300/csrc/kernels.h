@@ -9,6 +9,10 @@ namespace bl {
 
 struct Shape;
 
+// Limit (ns of global time) the kernels launched now give every bounded
+// device-side wait (bl_set_wait_limit; 2 s by default).
+uint64_t wait_limit_ns();
+
 // Forward + optional tile statistics (stats == nullptr skips them).
 cudaError_t launch_fwd(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                        float* lse, float* stats, float scale, cudaStream_t st);

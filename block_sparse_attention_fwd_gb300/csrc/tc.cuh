@@ -2,9 +2,13 @@
 // with bounded waits, TMA tensor loads, TMEM allocation, tcgen05.mma with
 // shared-memory descriptors, TMEM loads/stores and the fences between them.
 //
-// Every wait is bounded: after kWaitLimitNs of global time a wait gives up
-// and returns false, the caller records BL status bit kStatusTimeout and
-// skips the rest of its work so the kernel still ends and frees its TMEM.
+// Every wait is bounded: after the launch's limit (bl_set_wait_limit, 2 s by
+// default) a wait gives up and returns false, the caller records BL status
+// bit kStatusTimeout and skips the rest of its work.  Before a CTA in which a
+// wait gave up frees its TMEM and exits, the roles that issue asynchronous
+// work wait for it with the fixed kWaitLimitNs: the producer for the last
+// load of every barrier it armed, the MMA issuer for a commit behind its last
+// MMA; the storing warps always wait for their bulk groups.
 #pragma once
 
 #include <cuda.h>
@@ -89,7 +93,8 @@ __device__ __forceinline__ uint32_t mbar_test3(uint32_t a0, uint32_t p0, uint32_
       : "memory");
   return r;
 }
-// Wait for the phase with the given parity to complete; false after the limit.
+// Wait for the phase with the given parity to complete; false after
+// kWaitLimitNs of global time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = saddr(bar);
   if (mbar_try(a, parity)) return true;
@@ -98,6 +103,50 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_sleep(a, parity)) return true;
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
+}
+// The bounded wait of a kernel instantiation: the fixed limit, or (WL) the
+// launch's limit kept in shared memory at limit_smem.
+template <bool WL>
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity,
+                                           const uint64_t* limit_smem);
+template <>
+__device__ __forceinline__ bool wait_phase<false>(uint64_t* bar, uint32_t parity,
+                                                  const uint64_t*) {
+  return mbar_wait(bar, parity);
+}
+
+// Polling wait (no suspend hint) with the fixed limit, for the waits a CTA
+// that gave up makes before it exits.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = saddr(bar);
+  if (mbar_try(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_try(a, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+// The same with a limit set at launch (kept in shared memory, read only when
+// the phase is not complete at the first look).  Limits below the suspend
+// hint poll without sleeping, so a limit of 0 gives up on any phase that is
+// not complete at the second look.  Kernels instantiate this wait only for
+// launches under a non-default limit.
+__device__ __forceinline__ bool mbar_wait_limited(uint64_t* bar, uint32_t parity,
+                                                  const uint64_t* limit_smem) {
+  const uint32_t a = saddr(bar);
+  if (mbar_try(a, parity)) return true;
+  const uint64_t limit_ns = *reinterpret_cast<const volatile uint64_t*>(limit_smem);
+  const bool sleep = limit_ns >= kSuspendHintNs;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (sleep ? mbar_try_sleep(a, parity) : mbar_try(a, parity)) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+template <>
+__device__ __forceinline__ bool wait_phase<true>(uint64_t* bar, uint32_t parity,
+                                                 const uint64_t* limit_smem) {
+  return mbar_wait_limited(bar, parity, limit_smem);
 }
 
 // ---------------------------------------------------------------- TMA

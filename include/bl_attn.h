@@ -382,6 +382,19 @@ bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void*
 bl_status bl_varlen_bwd_check_status(const bl_varlen* varlen, const void* workspace,
                                      void* stream);
 
+/* Every device-side wait of the tcgen05 kernels (an mbarrier phase, a peer
+ * warp's hand-off) is bounded: when one runs out the kernel records it (the
+ * backward's status word: BL_ERR_TIMEOUT; the forward: NaN in the LSE rows it
+ * could not finish), skips the rest of its work, waits with a fixed 2 s
+ * limit for the copies and MMAs it already issued, frees its tensor memory
+ * and ends, so the context stays usable.  This sets the limit for kernels
+ * launched from now on, process-wide: seconds in [0, 2) (0 gives up on any
+ * wait that is not already satisfied), anything else restores the default of
+ * 2 s.  Returns the previous limit in seconds.  A diagnostic knob for testing
+ * the failure path; calls racing with launches in other threads see either
+ * value. */
+double bl_set_wait_limit(double seconds);
+
 /* Static description of a status code. */
 const char* bl_status_string(bl_status status);
 

@@ -400,3 +400,14 @@ def test_strided_shapes_are_validated_on_the_host(lib):
                 (1000 * 16 * 64, 16 * 64, 32, 1),      # heads overlap
                 (0, 16 * 64, 64, 1)):                  # non-positive
         assert _lib.tile_stats_elems(with_q(bad)) == 0
+
+
+def test_wait_limit_knob_clamps_and_restores(lib):
+    """bl_set_wait_limit (host only): [0, 2) s is taken as given, anything else
+    restores 2 s; each call returns the previous limit."""
+    from block_sparse_attention_fwd_gb300 import _lib
+    assert _lib.set_wait_limit(0.25) == pytest.approx(2.0)
+    assert _lib.set_wait_limit(5.0) == pytest.approx(0.25)
+    assert _lib.set_wait_limit(0.0) == pytest.approx(2.0)
+    assert _lib.set_wait_limit(-1.0) == 0.0
+    assert _lib.set_wait_limit(-1.0) == pytest.approx(2.0)
