@@ -471,57 +471,102 @@ def _active_flop(mask, w):
 
 def _e2e(args, w, shape, q, k, v, go, negl, dev):
     """Same step through the public API with host buffers: pinned H2D copies of
-    Q, K, V, G_O and D2H copies of G_Q, G_K, G_V inside the timed region.  G_O
-    is needed only by the backward, so it uploads on a copy stream while the
-    forward and the mask run; everything else is ordered on one stream."""
+    Q, K, V, G_O and D2H copies of G_Q, G_K, G_V inside the timed region, every
+    step.  The copies are pipelined with the compute like a loader's prefetch:
+    inputs and gradients are double-buffered on the device, step t+1's inputs
+    upload on one copy stream while step t computes, and step t's gradients
+    download on another while step t+1 computes; the timed region ends when the
+    last step's gradients have reached the host."""
     import torch
 
     from block_sparse_attention_fwd_gb300 import _lib
     hq, hk, hv, hg = (x.pin_memory() for x in (q, k, v, go))
-    outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q, k, v)]
-    dq, dk, dv, dg = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q, k, v, go))
-    o = torch.empty_like(dq)
+    outs = [[torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (q, k, v)]
+            for _ in range(2)]
+    ins = [[torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q, k, v, go)]
+           for _ in range(2)]
+    grads = [[torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q, k, v)]
+             for _ in range(2)]
+    o = torch.empty(q.shape, dtype=q.dtype, device=dev)
     lse = torch.empty((w.B, w.H, w.n), dtype=torch.float32, device=dev)
     T_r, T_c = _lib.tiles(shape)
     logw = torch.empty((w.B, w.H, T_r, T_c), dtype=torch.float32, device=dev)
     fws = torch.empty(_lib.fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
     lists = _lib.alloc_lists(shape, dev)
-    gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
     wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
-    go_ready = torch.cuda.Event()
+    main = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        copy.wait_stream(stream)                   # the previous step's backward read dg
-        with torch.cuda.stream(copy):
-            dg.copy_(hg, non_blocking=True)
-            go_ready.record(copy)
-        for dst, src in ((dq, hq), (dk, hk), (dv, hv)):
-            dst.copy_(src, non_blocking=True)
+    def upload(t):
+        i = t % 2
+        up.wait_event(computed[i])          # step t-2 has finished reading buffer i
+        with torch.cuda.stream(up):
+            for dst, src in zip(ins[i], (hq, hk, hv, hg)):
+                dst.copy_(src, non_blocking=True)
+            in_ready[i].record(up)
+
+    def compute(t):
+        i = t % 2
+        dq, dk, dv, dg = ins[i]
+        gq, gk, gv = grads[i]
+        main.wait_event(in_ready[i])
+        main.wait_event(downloaded[i])      # step t-2's gradients have left buffer i
         _lib.attn_fwd_tile_weights(shape, dq, dk, dv, w.scale, o, lse, logw, workspace=fws)
         _lib.mask_from_tile_weights(shape, logw, negl, lists)
-        stream.wait_event(go_ready)
         _lib.attn_bwd(shape, dq, dk, dv, o, dg, lse, w.scale, lists, gq, gk, gv, wsb)
-        for dst, src in zip(outs, (gq, gk, gv)):
-            dst.copy_(src, non_blocking=True)
+        computed[i].record(main)
 
-    for _ in range(2):
-        one()
+    def download(t):
+        i = t % 2
+        down.wait_event(computed[i])
+        with torch.cuda.stream(down):
+            for dst, src in zip(outs[i], grads[i]):
+                dst.copy_(src, non_blocking=True)
+            downloaded[i].record(down)
+
+    def run(n):
+        upload(0)
+        for t in range(n):
+            if t + 1 < n:
+                upload(t + 1)
+            compute(t)
+            download(t)
+        main.wait_stream(down)
+
+    for e in computed + downloaded:
+        e.record(main)
+    run(2)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    n = max(1, min(args.steps, 5))
-    a.record(stream)
-    for _ in range(n):
-        one()
-    b.record(stream)
+    n = max(2, min(args.steps, 6))
+    a.record(main)
+    run(n)
+    b.record(main)
     torch.cuda.synchronize()
     h2d = sum(x.numel() * x.element_size() for x in (q, k, v, go))
-    d2h = sum(x.numel() * x.element_size() for x in (gq, gk, gv))
-    return {"value": a.elapsed_time(b) / n, "unit": "ms", "what": "H2D inputs + fwd + mask + "
-            "bwd + D2H gradients, ms per step", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+    d2h = sum(x.numel() * x.element_size() for x in grads[0])
+    # the copy bandwidth alone (one direction at a time, same buffers)
+    bw = {}
+    for name, fn, nbytes in (("h2d", lambda: [d.copy_(s_, non_blocking=True) for d, s_ in
+                                              zip(ins[0], (hq, hk, hv, hg))], h2d),
+                             ("d2h", lambda: [d.copy_(s_, non_blocking=True) for d, s_ in
+                                              zip(outs[0], grads[0])], d2h)):
+        fn()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(main)
+        fn()
+        c1.record(main)
+        torch.cuda.synchronize()
+        bw[name + "_gbs"] = nbytes / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    return {"value": a.elapsed_time(b) / n, "unit": "ms",
+            "what": "H2D inputs + fwd + mask + bwd + D2H gradients, ms per step, the copies "
+                    "of neighbouring steps overlapped with the compute",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "copy_bandwidth": bw}
 
 
 def run_all_configs(args):
