@@ -379,7 +379,8 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": fwd_tf, "peak": pk["bf16"],
                      "unit": "TFLOP/s", "frac": fwd_tf / pk["bf16"],
                      "traffic": traffic.get("fwd_tc_kernel"),
-                     "kernel": "fwd_tc_kernel (4*B*H*n^2*d per launch)",
+                     "kernel": "fwd_tc_kernel with the tile-weight epilogue "
+                               "(4*B*H*n^2*d per launch)",
                      "peak_src": pk["src"] + " burst"},
         # the metric's own kernel: the block-sparse backward on computed tiles
         "roofline_bwd": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16"],
@@ -394,7 +395,8 @@ def run_ours(args):
                           "achieved": _mask_bytes(w, True) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
                           "peak": pk["hbm"], "unit": "GB/s",
                           "frac": _mask_bytes(w, True) / (statistics.mean(mask_ms) * 1e-3) / 1e9 / pk["hbm"],
-                          "traffic": None,
+                          "traffic": _sum_or_none(traffic, ("mask_rows_kernel_from_weights",
+                                                            "q_lists_kernel")),
                           "kernel": "bl_mask_from_tile_weights call (mask_rows_kernel + "
                                     "q_lists_kernel) reading the forward's tile weights"},
         "unfused": {"fwd_with_stats_ms": fwd_stats_ms, "mask_from_stats_ms": mask_stats_ms,
@@ -609,6 +611,14 @@ def run_all_configs(args):
         wsb = torch.empty(_lib.bwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
 
         reps = 3 if w.n >= 100000 else 5
+        # the tile-weights path (128 x 128 tiles): forward with the reduction
+        # epilogue, statistics rows in the scratch slots only
+        tw = _lib.fwd_workspace_bytes(shape) > 0
+        if tw:
+            logw = torch.empty((w.B, w.H, T_r, T_c), dtype=torch.float32, device=dev)
+            fws = torch.empty(_lib.fwd_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+            fwd_tw = timed(lambda: _lib.attn_fwd_tile_weights(shape, qd, kd, vd, w.scale, o, lse,
+                                                              logw, workspace=fws), reps)
         fwd = timed(lambda: _lib.attn_fwd(shape, qd, kd, vd, w.scale, o, lse, stats), reps)
         dense = timed(lambda: _lib.attn_bwd(shape, qd, kd, vd, o, god, lse, w.scale, None, g_q,
                                             g_k, g_v, wsb), reps)
@@ -619,6 +629,17 @@ def run_all_configs(args):
             mask = lists["mask"]
             skip = 1.0 - float(mask.float().mean())
             comp = _active_flop(mask, w)
+            tw_line = {}
+            if tw:
+                lists_w = _lib.alloc_lists(shape, dev)
+                mask_tw = timed(lambda: _lib.mask_from_tile_weights(shape, logw, negl, lists_w),
+                                reps)
+                if not torch.equal(lists_w["mask"], mask):
+                    raise RuntimeError(f"{name}: tile-weight mask differs from the stats mask")
+                tw_line = {"fwd_tw_ms": fwd_tw, "fwd_tw_frac_peak":
+                           w.dense_fwd_flop() / fwd_tw / 1e9 / pk["bf16"],
+                           "mask_tw_ms": mask_tw, "attn_bwd_tw_ms": mask_tw + bwd}
+                del lists_w
             line = {"workload": name, "negl_prob": negl, "fwd_ms": fwd,
                     "fwd_tflops": w.dense_fwd_flop() / fwd / 1e9,
                     "mask_ms": mask_ms, "mask_gbs": _mask_bytes(w) / mask_ms / 1e6,
@@ -627,7 +648,8 @@ def run_all_configs(args):
                     "skip_frac": skip,
                     "frac_bf16_peak_computed_tiles": comp / bwd / 1e9 / pk["bf16"],
                     "dense_bwd_ms": dense,
-                    "dense_bwd_frac_peak": w.dense_bwd_flop() / dense / 1e9 / pk["bf16"]}
+                    "dense_bwd_frac_peak": w.dense_bwd_flop() / dense / 1e9 / pk["bf16"],
+                    **tw_line}
             if not args.no_cpu_baseline:
                 ms_cpu, desc, tiles, el = cpu_reference_sample(w, q, k, v, go, budget_s=5.0,
                                                                max_tiles=64)
@@ -650,6 +672,8 @@ def run_all_configs(args):
                               "frac_hbm": nbytes / cm / 1e6 / pk["hbm"]}), flush=True)
             del op, lp, oc, lc
         del qd, kd, vd, god, o, lse, stats, lists, g_q, g_k, g_v, wsb
+        if tw:
+            del logw, fws
         torch.cuda.empty_cache()
     packed = [x for x in args.packed.split(",") if x] if args.packed else list(inputs.PACKED)
     for name in packed:

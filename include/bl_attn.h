@@ -319,9 +319,13 @@ bl_status bl_bwd_noalloc_check_status(const bl_shape* shape, void* stream);
  * the caller's stream with events, so that short sequences fill the GPU
  * together; the call returns with all its work ordered before anything the
  * caller enqueues next on its stream.  Nothing waits on the host, so the
- * calls can be captured in a CUDA graph.  lse only needs 4-byte alignment
- * here; the other device pointers need 16 bytes, as in the fixed-length
- * calls.
+ * calls can be captured in a CUDA graph.  The side streams belong to the
+ * library, one set per device shared by every caller: packed calls on
+ * different caller streams are serialised through them, and a packed call
+ * made while another thread captures a packed call on the same device would
+ * be recorded into that capture, so callers serialise packed calls that may
+ * overlap a capture on one device.  lse only needs 4-byte alignment here;
+ * the other device pointers need 16 bytes, as in the fixed-length calls.
  * ------------------------------------------------------------------------- */
 
 /* cu_seqlens: HOST array of nseq + 1 int32, cu_seqlens[0] = 0,
