@@ -218,6 +218,13 @@ def attn_fwd(shape, q, k, v, scale, o, lse, tile_stats=None):
     _check("bl_attn_fwd", code)
 
 
+def fwd_tile_weights_supported(shape: Shape) -> bool:
+    """Whether bl_attn_fwd_tile_weights takes this shape (the header's rule:
+    128 x 128 tiles, head dim 64 or 128, T_c <= 2048)."""
+    return (shape.block_q == 128 and shape.block_k == 128 and shape.d in (64, 128)
+            and tiles(shape)[1] <= 2048)
+
+
 def fwd_workspace_bytes(shape: Shape) -> int:
     """Scratch of attn_fwd_tile_weights without a statistics output (current device)."""
     return int(load().bl_fwd_workspace_bytes(ctypes.byref(shape)))

@@ -7,7 +7,9 @@ on (batch, seq_len, heads, head_dim) bf16 tensors, with key/value carrying
 ``heads_k`` heads.  With negl_prob > 0 the forward records tile statistics
 (allocating the buffer unless one is passed, README, Note) and the backward
 builds the block-sparse mask from them before running the sparse backward
-(How It Works, Phase 2).  negl_prob = 0 records nothing and runs the dense
+(How It Works, Phase 2).  With 128 x 128 tiles and no statistics buffer
+passed, the forward keeps only the tile weights d_ij the mask reads (the
+"Introducing BackLite" post, Using Sparsity), reduced in its epilogue.  negl_prob = 0 records nothing and runs the dense
 backward (Key properties).  ``BL_VERBOSE=1`` prints mask density per head
 after each mask pass (README, Debugging, names the same kind of switch).
 ``causal=True`` (optionally with ``window=W``) gives decoder attention, with
@@ -42,15 +44,24 @@ class _BLAttnFn(torch.autograd.Function):
         shape = _lib.make_shape(B, n, H, Hk, d, block_q, block_k, causal, window)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
-        stats = None
+        stats = logw = None
         if negl_prob > 0:
             T_r, T_c = _lib.tiles(shape)
-            want = (B, H, T_c, T_r * block_q)
-            stats = tile_stats if tile_stats is not None else torch.empty(
-                want, dtype=torch.float32, device=q.device)
-        _lib.attn_fwd(shape, q, k, v, scale, o, lse, stats)
+            if tile_stats is None and _lib.fwd_tile_weights_supported(shape):
+                # Only the T_r x T_c tile weights outlive the forward; the
+                # statistics rows stay in a scratch freed on return.
+                logw = torch.empty((B, H, T_r, T_c), dtype=torch.float32, device=q.device)
+                ws = torch.empty(_lib.fwd_workspace_bytes(shape), dtype=torch.uint8,
+                                 device=q.device)
+                _lib.attn_fwd_tile_weights(shape, q, k, v, scale, o, lse, logw, workspace=ws)
+            else:
+                want = (B, H, T_c, T_r * block_q)
+                stats = tile_stats if tile_stats is not None else torch.empty(
+                    want, dtype=torch.float32, device=q.device)
+        if logw is None:
+            _lib.attn_fwd(shape, q, k, v, scale, o, lse, stats)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.stats = stats
+        ctx.stats, ctx.logw = stats, logw
         ctx.cfg = (shape, scale, negl_prob)
         ctx.mark_non_differentiable(lse)
         return o, lse
@@ -61,9 +72,12 @@ class _BLAttnFn(torch.autograd.Function):
         shape, scale, negl_prob = ctx.cfg
         g_o = g_o.contiguous()
         lists = None
-        if ctx.stats is not None:
+        if ctx.stats is not None or ctx.logw is not None:
             lists = _lib.alloc_lists(shape, q.device)
-            _lib.mask_from_stats(shape, ctx.stats, lse, negl_prob, lists)
+            if ctx.logw is not None:
+                _lib.mask_from_tile_weights(shape, ctx.logw, negl_prob, lists)
+            else:
+                _lib.mask_from_stats(shape, ctx.stats, lse, negl_prob, lists)
             if os.environ.get("BL_VERBOSE") == "1":
                 m = lists["mask"].float()
                 dens = m.mean(dim=(2, 3)).cpu()

@@ -167,3 +167,31 @@ def test_autograd_module_runs_the_chain():
     for name, a, b in (("G_Q", qd.grad, rq), ("G_K", kd.grad, rk), ("G_V", vd.grad, rv)):
         e = U.rel_l2(U.cpu(a), b)
         assert e <= U.REL_L2, (name, e)
+
+
+def test_autograd_module_tile_weights_path():
+    """Without a statistics buffer the module's forward keeps only the tile
+    weights; its mask is the selection rule on the statistics the forward
+    would have written, so its gradients match the oracle's backward under
+    the mask of the statistics path on the same inputs."""
+    from block_sparse_attention_fwd_gb300 import BLAttention, _lib
+    w = inputs.custom("module_tw", B=1, n=1100, H=4, Hk=2, d=128, run=128, clusters=4)
+    q, k, v, go = inputs.generate(w)
+    shape = _lib.make_shape(w.B, w.n, w.H, w.Hk, w.d, 128, 128)
+    assert _lib.fwd_tile_weights_supported(shape)
+    T_r, T_c = _lib.tiles(shape)
+    attn = BLAttention(negl_prob=0.05)
+    stats = torch.empty((w.B, w.H, T_c, T_r * 128), dtype=torch.float32, device="cuda")
+    qs, ks, vs = (x.cuda().requires_grad_(True) for x in (q, k, v))
+    out_s, lse_s = attn(qs, ks, vs, return_softmax_lse=True, tile_stats=stats)
+    gm = U.oracle_mask(U.cpu(stats), U.cpu(lse_s), w.n, 128, 128, 0.05)["mask"]
+    assert 0 < float(gm.mean()) < 1
+    qd, kd, vd = (x.cuda().requires_grad_(True) for x in (q, k, v))
+    out, lse = attn(qd, kd, vd, return_softmax_lse=True)
+    out.backward(go.cuda())
+    assert torch.equal(out.detach(), out_s.detach())
+    assert torch.equal(lse, lse_s)
+    rq, rk, rv = A.backward(q, k, v, U.cpu(out.detach()), go, U.cpu(lse), w.scale, gm, 128, 128)
+    for name, a, b in (("G_Q", qd.grad, rq), ("G_K", kd.grad, rk), ("G_V", vd.grad, rv)):
+        e = U.rel_l2(U.cpu(a), b)
+        assert e <= U.REL_L2, (name, e)
