@@ -16,52 +16,80 @@ namespace bl {
 
 namespace {
 
-// D[b,h,r] = sum_d G_O[b,r,h,d] * O[b,r,h,d]: one warp per (b, r, h) row.
-// The same warp zeroes that row of the fp32 dQ accumulator, and block 0 the
-// status word and the word after it (the tcgen05 backward's work-item
-// counter), so no separate memset pass is needed.
+// D[b,h,r] = sum_d G_O[b,r,h,d] * O[b,r,h,d].  One warp per (b, block of 32
+// rows r, h), h fastest, so the eight warps of a block read neighbouring
+// heads of the same rows.  D / 8 lanes share a row (16 bytes of O and of G_O
+// each), and 32 / (D / 8) rows go per step; the loads of four steps are in
+// flight together.  Lane l keeps D of row r0 + l, so the warp writes its 32
+// values with one coalesced store.  The warp also zeroes its rows of the fp32
+// dQ accumulator, and block 0 the status word and the word after it (the
+// tcgen05 backward's work-item counter), so no separate memset pass is needed.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ g_o,
                                                       float* __restrict__ Dv,
                                                       float* __restrict__ dq_acc,
                                                       int32_t* __restrict__ status, Shape sh) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  constexpr int LPR = D / 8;        // lanes per row
+  constexpr int RPS = 32 / LPR;     // rows per step
+  constexpr int STEPS = 32 / RPS;
+  constexpr int U = 4;              // steps whose loads are in flight together
   const int lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)sh.B * sh.n * sh.H;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     status[0] = 0;
     status[1] = 0;
   }
-  if (row >= total) return;
-  {
-    float* z = dq_acc + row * D + lane * (D / 32);
-    if constexpr (D == 128)
-      *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else
-      *reinterpret_cast<float2*>(z) = make_float2(0.f, 0.f);
-  }
-  constexpr int E = D / 32;  // elements per lane (2 or 4)
-  const int rh = (int)(row % sh.H);
-  const int64_t rbr = row / sh.H;
-  const int64_t ro = bshd(sh.os, (int)(rbr / sh.n), (int)(rbr % sh.n), rh);
-  const __nv_bfloat16* op = o + ro + lane * E;
-  const __nv_bfloat16* gp = g_o + ro + lane * E;
-  float acc = 0.f;
+  const int nblk = (sh.n + 31) / 32;
+  const int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (w >= (int64_t)sh.B * nblk * sh.H) return;
+  const int h = (int)(w % sh.H);
+  const int64_t br = w / sh.H;
+  const int b = (int)(br / nblk);
+  const int r0 = (int)(br % nblk) * 32;
+  const int sub = lane / LPR, c8 = (lane % LPR) * 8;
+  float d_mine = 0.f;
 #pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(op + e));
-    float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(gp + e));
-    acc += a.x * c.x + a.y * c.y;
-  }
+  for (int s0 = 0; s0 < STEPS; s0 += U) {
+    uint4 ov[U], gv[U];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    int h = (int)(row % sh.H);
-    int64_t br = row / sh.H;
-    int r = (int)(br % sh.n);
-    int b = (int)(br / sh.n);
-    Dv[((int64_t)b * sh.H + h) * sh.n + r] = acc;
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + (s0 + u) * RPS + sub;
+      ov[u] = make_uint4(0u, 0u, 0u, 0u);
+      gv[u] = ov[u];
+      if (r < sh.n) {
+        const int64_t off = bshd(sh.os, b, r, h) + c8;
+        ov[u] = *reinterpret_cast<const uint4*>(o + off);
+        gv[u] = *reinterpret_cast<const uint4*>(g_o + off);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t* a = reinterpret_cast<const uint32_t*>(&ov[u]);
+      const uint32_t* c = reinterpret_cast<const uint32_t*>(&gv[u]);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a[e]));
+        const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&c[e]));
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      // row (s0 + u) * RPS + i sits in lanes i * LPR ...; lane l takes row l
+      const float v = __shfl_sync(0xffffffffu, acc, (lane % RPS) * LPR);
+      if (lane / RPS == s0 + u) d_mine = v;
+    }
+  }
+  if (r0 + lane < sh.n) Dv[((int64_t)b * sh.H + h) * sh.n + r0 + lane] = d_mine;
+  // zero the accumulator rows (b, r0..r0+31, h): D fp32 = D / 4 float4 per row
+  constexpr int F4 = D / 4;
+#pragma unroll 4
+  for (int x = lane; x < 32 * F4; x += 32) {
+    const int r = r0 + x / F4;
+    if (r < sh.n)
+      reinterpret_cast<float4*>(dq_acc + (((int64_t)b * sh.n + r) * sh.H + h) * D)[x % F4] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -96,7 +124,8 @@ cudaError_t launch_bwd(const Shape& sh, const void* q, const void* k, const void
                        void* g_v, float* ws_D, float* ws_dq, int32_t* ws_sub,
                        int32_t* ws_status, cudaStream_t st) {
   const int64_t rows = (int64_t)sh.B * sh.n * sh.H;
-  unsigned pre_blocks = (unsigned)((rows + 7) / 8);
+  const int64_t pre_warps = (int64_t)sh.B * ((sh.n + 31) / 32) * sh.H;
+  unsigned pre_blocks = (unsigned)((pre_warps + 7) / 8);
   if (sh.d == 64)
     bwd_pre_kernel<64><<<pre_blocks, 256, 0, st>>>((const __nv_bfloat16*)o,
                                                    (const __nv_bfloat16*)g_o, ws_D, ws_dq,
