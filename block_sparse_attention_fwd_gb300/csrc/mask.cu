@@ -291,6 +291,133 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
   if (tid == 0) kv_cnt[bh * sh.T_r + i] = cnt_run;
 }
 
+// The same rule from the tile weights for T_c <= 256, one warp per query
+// tile: lane l holds entries 8 l .. 8 l + 7 of the row.  The bitonic network
+// over the 256 (key, j) pairs swaps within a lane for strides below 8 and
+// across lanes (shuffles) above; d comes back from the sorted key itself
+// (order_key is invertible), so nothing but the mask bytes passes through
+// shared memory.  Eight rows per block, no block-wide barrier.
+__device__ __forceinline__ float key_to_d(unsigned long long key) {
+  const uint32_t k = (uint32_t)(key >> 32);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__global__ void __launch_bounds__(256) mask_rows_warp_kernel(
+    const float* __restrict__ logw, Shape sh, unsigned long long T, uint8_t* __restrict__ mask,
+    int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
+    int32_t* __restrict__ nan_count) {
+  __shared__ __align__(8) uint8_t s_act[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
+  if (row >= (int64_t)sh.B * sh.H * sh.T_r) return;
+  const int i = (int)(row % sh.T_r);
+  const int Tc = sh.T_c;
+  int k_lo, k_hi;
+  key_tile_range(sh, i, k_lo, k_hi);
+  const float* wrow = logw + row * (int64_t)Tc;
+  uint8_t* act = s_act[warp];
+  unsigned long long key[8];
+  int local_nan = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int m = lane * 8 + e;
+    key[e] = ~0ull;
+    if (m < Tc) {
+      const float dv = wrow[m];
+      if (isnan(dv)) {
+        key[e] = (0xffffffffull << 32) | (unsigned)m;
+        ++local_nan;
+      } else {
+        key[e] = ((unsigned long long)order_key(dv) << 32) | (unsigned)m;
+      }
+    }
+    act[m] = m < Tc;
+  }
+  if (nan_count) {
+    local_nan = __reduce_add_sync(0xffffffffu, local_nan);
+    if (lane == 0 && local_nan) atomicAdd(nan_count, local_nan);
+  }
+  // bitonic sort ascending of the 256 keys (unique but for the padding)
+#pragma unroll
+  for (int kk = 2; kk <= 256; kk <<= 1) {
+#pragma unroll
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      if (jj < 8) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (e & jj) continue;
+          const bool up = ((lane * 8 + e) & kk) == 0;
+          const unsigned long long a = key[e], c = key[e | jj];
+          const bool sw = (a > c) == up;
+          key[e] = sw ? c : a;
+          key[e | jj] = sw ? a : c;
+        }
+      } else {
+        const int lj = jj >> 3;
+        const bool lower = (lane & lj) == 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const unsigned long long pk = __shfl_xor_sync(0xffffffffu, key[e], lj);
+          const bool up = ((lane * 8 + e) & kk) == 0;
+          // the lower element of an ascending pair keeps the smaller key
+          if ((lower == up) ? (pk < key[e]) : (pk > key[e])) key[e] = pk;
+        }
+      }
+    }
+  }
+  // inclusive prefix of E in sorted order; the skipped entries are the
+  // non-NaN positions whose prefix stays below T (a prefix of the order)
+  unsigned long long E[8], tot = 0ull;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    E[e] = (key[e] >> 32) != 0xffffffffull ? detexp_fixed40(key_to_d(key[e])) : 0ull;
+    tot += E[e];
+  }
+  unsigned long long incl = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  unsigned long long pre = incl - tot;
+  __syncwarp();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    pre += E[e];
+    if ((key[e] >> 32) != 0xffffffffull && pre < T) act[(int)(key[e] & 0xffffffffull)] = 0;
+  }
+  __syncwarp();
+  // the mask row (8 bytes per lane) and the ascending kv list
+  const uint2 a8 = *reinterpret_cast<const uint2*>(act + lane * 8);
+  uint8_t f[8];
+  int mine = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int m = lane * 8 + e;
+    const uint32_t byte = ((e < 4 ? a8.x : a8.y) >> (8 * (e & 3))) & 0xffu;
+    f[e] = (uint8_t)(byte && m >= k_lo && m <= k_hi);
+    mine += f[e];
+  }
+  uint8_t* mrow = mask + row * (int64_t)Tc;
+  int32_t* krow = kv_idx + row * (int64_t)Tc;
+  int off = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, off, o);
+    if (lane >= o) off += y;
+  }
+  const int cnt = __shfl_sync(0xffffffffu, off, 31);
+  off -= mine;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int m = lane * 8 + e;
+    if (m < Tc) mrow[m] = f[e];
+    if (f[e]) krow[off++] = m;
+  }
+  for (int j = cnt + lane; j < Tc; j += 32) krow[j] = -1;
+  if (lane == 0) kv_cnt[row] = cnt;
+}
+
 __global__ void __launch_bounds__(256) q_lists_kernel(const uint8_t* __restrict__ mask, Shape sh,
                                                       int32_t* __restrict__ q_idx,
                                                       int32_t* __restrict__ q_cnt) {
@@ -326,7 +453,11 @@ cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
       mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value, false>
           <<<g1, kMaskThreads, 0, st>>>(stats, lse, nullptr, sh, threshold, mask, kv_idx, kv_cnt,
                                         nan_count);
-    else
+    else if (decltype(cap)::value == 256) {
+      const int64_t rows_all = (int64_t)sh.B * sh.H * sh.T_r;
+      mask_rows_warp_kernel<<<(unsigned)((rows_all + 7) / 8), 256, 0, st>>>(
+          logw, sh, threshold, mask, kv_idx, kv_cnt, nan_count);
+    } else
       mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value, true>
           <<<g1, kMaskThreads, 0, st>>>(nullptr, nullptr, logw, sh, threshold, mask, kv_idx,
                                         kv_cnt, nan_count);
