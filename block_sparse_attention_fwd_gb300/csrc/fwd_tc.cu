@@ -327,27 +327,42 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
           if (c > c_hi || c < c_lo) x[c] = __float_as_uint(-INFINITY);
       }
       // max over the raw scores (the scale is positive), in base-2 units
-      float mr = __uint_as_float(x[0]);
+      float mr = fmaxf(__uint_as_float(x[0]), __uint_as_float(x[1]));
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mr = fmaxf(mr, __uint_as_float(x[c]));
+      for (int c = 2; c < 128; c += 2)
+        mr = fmax3(mr, __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
       const float mt = mr * scale_log2;
       const bool grow = mt > m_ref + C::kRescale;
       const float m_new = grow ? mt : m_ref;
       const float alpha = grow ? fast_exp2(m_ref - m_new) : 1.f;
       // a row that has attended no key yet keeps m = -inf: its p are 0
       const float m_sub = m_new == -INFINITY ? 0.f : m_new;
-      float ts = 0.f, ts_lo = 0.f;
-      // p = 2^(x s log2 e - m); bf16 pairs packed in place (entry c from 2c, 2c+1)
+      // p = 2^(x s log2 e - m); bf16 pairs packed in place (entry c from 2c,
+      // 2c+1).  Arguments and row sums go two columns per instruction: the
+      // even and the odd columns' p are summed separately.
+      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_sub, -m_sub);
+      uint64_t ts2 = f2_pack(0.f, 0.f), ts2_lo = ts2;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), scale_log2, -m_sub));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), scale_log2, -m_sub));
+        float a0, a1;
+        f2_unpack(ffma2(f2_pack(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1])), sc2,
+                        nm2),
+                  a0, a1);
+        const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
         if (SUB == 2 && c == 32) {   // keys 0-63 and 64-127: two 64-key tiles
-          ts_lo = ts;
-          ts = 0.f;
+          ts2_lo = ts2;
+          ts2 = f2_pack(0.f, 0.f);
         }
-        ts += p0 + p1;
+        ts2 = fadd2(ts2, f2_pack(p0, p1));
         x[c] = pack_bf16(p0, p1);
+      }
+      float ts, ts_lo;
+      {
+        float u0, u1;
+        f2_unpack(ts2, u0, u1);
+        ts = u0 + u1;
+        f2_unpack(ts2_lo, u0, u1);
+        ts_lo = u0 + u1;
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c)
