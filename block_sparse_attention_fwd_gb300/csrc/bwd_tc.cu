@@ -95,7 +95,7 @@ struct Cfg {
   static constexpr int OFF_RING = OFF_V + TILE;
   static constexpr int OFF_DS = OFF_RING + NS * TILE;
   static constexpr int OFF_STAGE = OFF_DS + DS_BYTES;
-  static constexpr int OFF_L = OFF_STAGE + STAGE_BYTES;   // NS x 128 floats: lse*log2e
+  static constexpr int OFF_L = OFF_STAGE + STAGE_BYTES;   // NS x 128 floats: -lse*log2e
   static constexpr int OFF_D = OFF_L + NS * 128 * 4;      // NS x 128 floats: D
   static constexpr int OFF_LIST = OFF_D + NS * 128 * 4;   // 2 x LIST_CAP ints
   static constexpr int OFF_LCNT = OFF_LIST + 2 * LIST_CAP * 4;
@@ -314,12 +314,12 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         for (int which = 0; which < 2 && ok; ++which, ++x) {
           const int s = slot_of(x);
           float lv[4], dv[4];
-          if (which == 0) {   // this tile's LSE and D travel with its Q slot
+          if (which == 0) {   // this tile's -LSE log2(e) and D travel with its Q slot
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int r = r0 + lane + 32 * e;
               const bool in = r < sh.n;
-              lv[e] = in ? lse[bh * sh.n + r] * kLog2e : INFINITY;
+              lv[e] = in ? -(lse[bh * sh.n + r] * kLog2e) : -INFINITY;
               dv[e] = in ? Dv[bh * sh.n + r] : 0.f;
             }
           }
@@ -565,6 +565,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     const int r = q4 * 32 + lane;               // key row within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     uint8_t* ds_row = sm + C::OFF_DS + half * C::CHUNK + r * 128;
+    const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     int t = 0, kk = 0;
     bool ok = true;
     bool store_pending = false;   // this warp's dK/dV rows may still be read from ds_row
@@ -608,15 +609,19 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
             uint32_t sv[16];
             tmem_ld16(lane_base + C::T_S + half * 64 + c0, sv);
             tmem_ld_wait();
+            // two columns per fma: s S^T log2(e) - LSE log2(e) (sl holds the negation)
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
               const float4 l4 = reinterpret_cast<const float4*>(sl + c0)[c4];
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-              for (int y = 0; y < 4; ++y) {
+              for (int y = 0; y < 4; y += 2) {
                 const int c = 4 * c4 + y;
-                pf[c0 + c] =
-                    key_on ? fast_exp2(fmaf(__uint_as_float(sv[c]), scale_log2, -lv[y])) : 0.f;
+                float a0, a1;
+                f2_unpack(ffma2(f2_pack(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2,
+                                y == 0 ? f2_pack(l4.x, l4.y) : f2_pack(l4.z, l4.w)),
+                          a0, a1);
+                pf[c0 + c] = key_on ? fast_exp2(a0) : 0.f;
+                pf[c0 + c + 1] = key_on ? fast_exp2(a1) : 0.f;
               }
             }
             if (diag) {
@@ -649,18 +654,20 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
           tmem_ld16(lane_base + C::T_DP + half * 64 + pass * 16, pv);
           tmem_ld_wait();
           uint32_t dk[8];
+          // dS^T = P^T (dP^T - D), two columns per instruction
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const float4 d4 = reinterpret_cast<const float4*>(sd + pass * 16)[c4];
-            const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float ds[4];
 #pragma unroll
-            for (int y = 0; y < 4; ++y) {
+            for (int y = 0; y < 4; y += 2) {
               const int c = 4 * c4 + y;
-              ds[y] = pf[pass * 16 + c] * (__uint_as_float(pv[c]) - dv[y]);
+              float s0, s1;
+              f2_unpack(fmul2(f2_pack(pf[pass * 16 + c], pf[pass * 16 + c + 1]),
+                              fsub2(f2_pack(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                    y == 0 ? f2_pack(d4.x, d4.y) : f2_pack(d4.z, d4.w))),
+                        s0, s1);
+              dk[2 * c4 + y / 2] = pack_bf16(s0, s1);
             }
-            dk[2 * c4] = pack_bf16(ds[0], ds[1]);
-            dk[2 * c4 + 1] = pack_bf16(ds[2], ds[3]);
           }
           // dS^T, K-major [key][q] with the 128-byte swizzle, 2 x 16 B chunks
 #pragma unroll
