@@ -395,9 +395,9 @@ def run_ours(args):
                           "achieved": _mask_bytes(w, True) / (statistics.mean(mask_ms) * 1e-3) / 1e9,
                           "peak": pk["hbm"], "unit": "GB/s",
                           "frac": _mask_bytes(w, True) / (statistics.mean(mask_ms) * 1e-3) / 1e9 / pk["hbm"],
-                          "traffic": _sum_or_none(traffic, ("mask_rows_kernel_from_weights",
+                          "traffic": _sum_or_none(traffic, ("mask_rows_warp_kernel",
                                                             "q_lists_kernel")),
-                          "kernel": "bl_mask_from_tile_weights call (mask_rows_kernel + "
+                          "kernel": "bl_mask_from_tile_weights call (mask_rows_warp_kernel + "
                                     "q_lists_kernel) reading the forward's tile weights"},
         "unfused": {"fwd_with_stats_ms": fwd_stats_ms, "mask_from_stats_ms": mask_stats_ms,
                     "mask_from_stats_gbs": _mask_bytes(w) / (mask_stats_ms * 1e-3) / 1e9,

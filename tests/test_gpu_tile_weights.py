@@ -96,19 +96,21 @@ def test_tile_weights_match_the_oracle_and_the_stats_path(w):
         U.assert_lists_equal(a, ref_lists)
 
 
-def test_tile_weights_mask_on_planted_weights():
+@pytest.mark.parametrize("n", [1024, 640, 32768, 38400])
+def test_tile_weights_mask_on_planted_weights(n):
     """Hand-built weights with ties, -inf and NaN tiles: the mask from the
-    weights is the oracle's selection of exactly those rows."""
+    weights is the oracle's selection of exactly those rows.  T_c = 8, 5 and
+    256 run the one-warp-per-row kernel, T_c = 300 the block-per-row one."""
     from block_sparse_attention_fwd_gb300 import _lib
-    B, H, n = 1, 2, 1024
+    B, H = 1, 2
     shape = _lib.make_shape(B, n, H, H, 128, 128, 128)
     T = n // 128
     rng = np.random.default_rng(11)
     d = np.log(rng.dirichlet(np.full(T, 0.4), size=(B, H, T))).astype(np.float32)
     d = np.minimum(d, 0).astype(np.float32)
     d[0, 0, 2, 1] = d[0, 0, 2, 0]                 # tie
-    d[0, 1, 3, 5] = -np.inf                      # empty tile
-    d[0, 1, 4, 6] = np.nan                       # NaN weight
+    d[0, 1, 3, min(5, T - 1)] = -np.inf          # empty tile
+    d[0, 1, 4, min(6, T - 2)] = np.nan           # NaN weight
     lw = torch.from_numpy(d).cuda()
     for negl in (0.0, 0.02, 0.2, 0.9):
         lists = _lib.alloc_lists(shape, "cuda")
