@@ -239,7 +239,9 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
           mma_ss(tmem + C::T_S + t * 128, sdesc_sw128(qb + off, 16, 1024),
                  sdesc_sw128(kb + off, 16, 1024), C::ID_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars.s_full[t]);
+        // S_B's completion is signalled by the key tile's done commit, which
+        // follows it: one commit fewer per key tile for the issuing thread
+        if (t == 0) mma_commit(&bars.s_full[0]);
       };
       auto issue_pv = [&](int t, int jj) {  // O_t += P_t V of visit jj, P_t read from TMEM
         const uint32_t vb = sV + (jj % C::NV) * C::TILE_BYTES;
@@ -307,8 +309,11 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     bool ok = valid_tile;
     for (int jj = 0; ok && jj < nj; ++jj) {
       const int j = j_lo + jj;
+      // S_A(jj) signals s_full[0]; S_B(jj) the done commit of visit jj
       ok = __all_sync(0xffffffffu,
-                      !failed(&s_fail) && wait_phase<WL>(&bars.s_full[t], jj & 1, &s_wait));
+                      !failed(&s_fail) &&
+                          (t == 0 ? wait_phase<WL>(&bars.s_full[0], jj & 1, &s_wait)
+                                  : wait_phase<WL>(&bars.done[jj % 3], (jj / 3) & 1, &s_wait)));
       if (!ok) break;
       fence_after_sync();
       uint32_t x[128];
