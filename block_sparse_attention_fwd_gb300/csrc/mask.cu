@@ -292,13 +292,16 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
 }
 
 // The same rule from the tile weights for T_c <= 256, one warp per query
-// tile: lane l holds entries 8 l .. 8 l + 7 of the row.  The bitonic network
-// over the 256 (key, j) pairs swaps within a lane for strides below 8 and
-// across lanes (shuffles) above; d comes back from the sorted key itself
-// (order_key is invertible), so nothing but the mask bytes passes through
-// shared memory.  Eight rows per block, no block-wide barrier.
-__device__ __forceinline__ float key_to_d(unsigned long long key) {
-  const uint32_t k = (uint32_t)(key >> 32);
+// tile: lane l holds entries 8 l .. 8 l + 7 of the row (entry = key tile j).
+// Only the 32-bit order keys of d are sorted (bitonic network: strides below
+// 8 swap within a lane, the others through shuffles), which fixes the
+// position nskip where the skipped prefix ends and the key K* of its last
+// entry.  Ties in d carry equal E, so the prefix sums, hence nskip, do not
+// depend on how the network orders them; the skipped entries in (d asc,
+// j asc) order are then every j with key < K* and, of the j with key == K*,
+// the lowest r = nskip - #(key < K*), ranked by j with a warp scan.  Eight
+// rows per block, no shared memory, no block barrier.
+__device__ __forceinline__ float key_to_d(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
     const float* __restrict__ logw, Shape sh, unsigned long long T, uint8_t* __restrict__ mask,
     int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
     int32_t* __restrict__ nan_count) {
-  __shared__ __align__(8) uint8_t s_act[8][256];
+  constexpr uint32_t kLast = 0xffffffffu;   // NaN weights and padding: sorted last, E = 0
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + warp;
   if (row >= (int64_t)sh.B * sh.H * sh.T_r) return;
@@ -315,29 +318,25 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
   int k_lo, k_hi;
   key_tile_range(sh, i, k_lo, k_hi);
   const float* wrow = logw + row * (int64_t)Tc;
-  uint8_t* act = s_act[warp];
-  unsigned long long key[8];
+  uint32_t orig[8], key[8];
   int local_nan = 0;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int m = lane * 8 + e;
-    key[e] = ~0ull;
+    orig[e] = kLast;
     if (m < Tc) {
       const float dv = wrow[m];
-      if (isnan(dv)) {
-        key[e] = (0xffffffffull << 32) | (unsigned)m;
+      if (isnan(dv))
         ++local_nan;
-      } else {
-        key[e] = ((unsigned long long)order_key(dv) << 32) | (unsigned)m;
-      }
+      else
+        orig[e] = order_key(dv);
     }
-    act[m] = m < Tc;
+    key[e] = orig[e];
   }
   if (nan_count) {
     local_nan = __reduce_add_sync(0xffffffffu, local_nan);
     if (lane == 0 && local_nan) atomicAdd(nan_count, local_nan);
   }
-  // bitonic sort ascending of the 256 keys (unique but for the padding)
 #pragma unroll
   for (int kk = 2; kk <= 256; kk <<= 1) {
 #pragma unroll
@@ -347,30 +346,29 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
         for (int e = 0; e < 8; ++e) {
           if (e & jj) continue;
           const bool up = ((lane * 8 + e) & kk) == 0;
-          const unsigned long long a = key[e], c = key[e | jj];
-          const bool sw = (a > c) == up;
-          key[e] = sw ? c : a;
-          key[e | jj] = sw ? a : c;
+          const uint32_t lo = min(key[e], key[e | jj]), hi = max(key[e], key[e | jj]);
+          key[e] = up ? lo : hi;
+          key[e | jj] = up ? hi : lo;
         }
       } else {
         const int lj = jj >> 3;
         const bool lower = (lane & lj) == 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const unsigned long long pk = __shfl_xor_sync(0xffffffffu, key[e], lj);
+          const uint32_t pk = __shfl_xor_sync(0xffffffffu, key[e], lj);
           const bool up = ((lane * 8 + e) & kk) == 0;
           // the lower element of an ascending pair keeps the smaller key
-          if ((lower == up) ? (pk < key[e]) : (pk > key[e])) key[e] = pk;
+          key[e] = (lower == up) ? min(key[e], pk) : max(key[e], pk);
         }
       }
     }
   }
-  // inclusive prefix of E in sorted order; the skipped entries are the
-  // non-NaN positions whose prefix stays below T (a prefix of the order)
+  // inclusive prefix of E in sorted order: nskip = the non-NaN positions whose
+  // prefix stays below T (a prefix of the order)
   unsigned long long E[8], tot = 0ull;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    E[e] = (key[e] >> 32) != 0xffffffffull ? detexp_fixed40(key_to_d(key[e])) : 0ull;
+    E[e] = key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
     tot += E[e];
   }
   unsigned long long incl = tot;
@@ -380,24 +378,56 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
     if (lane >= off) incl += y;
   }
   unsigned long long pre = incl - tot;
-  __syncwarp();
+  int nskip = 0;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     pre += E[e];
-    if ((key[e] >> 32) != 0xffffffffull && pre < T) act[(int)(key[e] & 0xffffffffull)] = 0;
+    nskip += (key[e] != kLast && pre < T);
   }
-  __syncwarp();
-  // the mask row (8 bytes per lane) and the ascending kv list
-  const uint2 a8 = *reinterpret_cast<const uint2*>(act + lane * 8);
-  uint8_t f[8];
-  int mine = 0;
+  nskip = __reduce_add_sync(0xffffffffu, nskip);
+  // K*: the sorted key at position nskip - 1; r of its ties are skipped
+  uint32_t kstar = 0u;
+  int r = 0;
+  if (nskip > 0) {
+    const int p = nskip - 1;
+    const int pe = p & 7;   // a select tree keeps key[] in registers
+    const uint32_t mine =
+        pe < 4 ? (pe < 2 ? (pe == 0 ? key[0] : key[1]) : (pe == 2 ? key[2] : key[3]))
+               : (pe < 6 ? (pe == 4 ? key[4] : key[5]) : (pe == 6 ? key[6] : key[7]));
+    kstar = __shfl_sync(0xffffffffu, mine, p >> 3);
+    int less = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) less += orig[e] < kstar;
+    r = nskip - __reduce_add_sync(0xffffffffu, less);
+  }
+  // rank of each tie (key == K*) by j: warp exclusive scan of the per-lane counts
+  int ties = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ties += (nskip > 0 && orig[e] == kstar);
+  int tie_off = ties;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, tie_off, o);
+    if (lane >= o) tie_off += y;
+  }
+  tie_off -= ties;
+  // the mask row and the ascending kv list
+  uint32_t fbits = 0u;   // bit e: entry 8 lane + e is kept
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int m = lane * 8 + e;
-    const uint32_t byte = ((e < 4 ? a8.x : a8.y) >> (8 * (e & 3))) & 0xffu;
-    f[e] = (uint8_t)(byte && m >= k_lo && m <= k_hi);
-    mine += f[e];
+    bool skip = false;
+    if (nskip > 0) {
+      if (orig[e] < kstar) {
+        skip = true;
+      } else if (orig[e] == kstar) {
+        skip = tie_off < r;
+        ++tie_off;
+      }
+    }
+    if (m < Tc && !skip && m >= k_lo && m <= k_hi) fbits |= 1u << e;
   }
+  const int mine = __popc(fbits);
   uint8_t* mrow = mask + row * (int64_t)Tc;
   int32_t* krow = kv_idx + row * (int64_t)Tc;
   int off = mine;
@@ -411,8 +441,9 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const int m = lane * 8 + e;
-    if (m < Tc) mrow[m] = f[e];
-    if (f[e]) krow[off++] = m;
+    const uint32_t fe = (fbits >> e) & 1u;
+    if (m < Tc) mrow[m] = (uint8_t)fe;
+    if (fe) krow[off++] = m;
   }
   for (int j = cnt + lane; j < Tc; j += 32) krow[j] = -1;
   if (lane == 0) kv_cnt[row] = cnt;
