@@ -81,12 +81,10 @@ __device__ __forceinline__ uint32_t order_key(float d) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// FROM_W: d_ij comes ready-made from the tile weights logw [B,H,T_r,T_c] that
-// the forward reduced (the same arithmetic as the reduction below).
-template <int RPL, int CAP, bool FROM_W>  // rows per lane: block_q / 32; capacity >= T_c
+template <int RPL, int CAP>  // rows per lane: block_q / 32; capacity >= T_c
 __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
-    const float* __restrict__ stats, const float* __restrict__ lse,
-    const float* __restrict__ logw, Shape sh, unsigned long long T, uint8_t* __restrict__ mask,
+    const float* __restrict__ stats, const float* __restrict__ lse, Shape sh,
+    unsigned long long T, uint8_t* __restrict__ mask,
     int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
     int32_t* __restrict__ nan_count) {
   __shared__ float s_d[CAP];
@@ -102,10 +100,7 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
   const int64_t bh = (int64_t)b * sh.H + h;
   int k_lo, k_hi;
   key_tile_range(sh, i, k_lo, k_hi);
-  if constexpr (FROM_W) {
-    const float* wrow = logw + (bh * sh.T_r + i) * (int64_t)Tc;
-    for (int j = tid; j < Tc; j += kMaskThreads) s_d[j] = wrow[j];
-  } else {
+  {
     const int r0 = i * sh.block_q + lane * RPL;
     float lrow[RPL];
     bool valid[RPL];
@@ -291,72 +286,99 @@ __global__ void __launch_bounds__(kMaskThreads) mask_rows_kernel(
   if (tid == 0) kv_cnt[bh * sh.T_r + i] = cnt_run;
 }
 
-// The same rule from the tile weights for T_c <= 256, one warp per query
-// tile: lane l holds entries 8 l .. 8 l + 7 of the row (entry = key tile j).
-// Only the 32-bit order keys of d are sorted (bitonic network: strides below
-// 8 swap within a lane, the others through shuffles), which fixes the
-// position nskip where the skipped prefix ends and the key K* of its last
-// entry.  Ties in d carry equal E, so the prefix sums, hence nskip, do not
-// depend on how the network orders them; the skipped entries in (d asc,
-// j asc) order are then every j with key < K* and, of the j with key == K*,
-// the lowest r = nskip - #(key < K*), ranked by j with a warp scan.  Eight
-// rows per block, no shared memory, no block barrier.
+// The same rule from the tile weights, one warp per query tile: lane l holds
+// entries PER l .. PER l + PER - 1 of the row (entry = key tile j; PER =
+// 8, 16, 32 or 64 for T_c up to 256, 512, 1024, 2048).  Only the 32-bit
+// order keys of d are sorted (bitonic network: strides below PER swap within
+// a lane, the others through shuffles), which fixes the position nskip where
+// the skipped prefix ends and the key K* of its last entry.  Ties in d carry
+// equal E, so the prefix sums, hence nskip, do not depend on how the network
+// orders them; the skipped entries in (d asc, j asc) order are then every j
+// with key < K* and, of the j with key == K*, the lowest r = nskip -
+// #(key < K*), ranked by j with a warp scan.  No shared memory, no block
+// barrier.
 __device__ __forceinline__ float key_to_d(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__global__ void __launch_bounds__(256) mask_rows_warp_kernel(
+// k[idx] for a register array through a select tree (a loop of conditional
+// moves would let the compiler move the array to local memory)
+template <int LO, int HI>
+__device__ __forceinline__ uint32_t pick(const uint32_t* k, int idx) {
+  if constexpr (HI - LO == 1) {
+    return k[LO];
+  } else {
+    constexpr int MID = (LO + HI) / 2;
+    return idx < MID ? pick<LO, MID>(k, idx) : pick<MID, HI>(k, idx);
+  }
+}
+
+// rows (warps) per block: eight for the small rows; two where a warp holds
+// many registers, so that more of them fit on an SM
+template <int PER>
+constexpr int kWarpRows = PER <= 8 ? 8 : 2;
+
+template <int PER>
+__global__ void __launch_bounds__(32 * kWarpRows<PER>) mask_rows_warp_kernel(
     const float* __restrict__ logw, Shape sh, unsigned long long T, uint8_t* __restrict__ mask,
     int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
     int32_t* __restrict__ nan_count) {
+  constexpr int N = 32 * PER;               // sorted entries (padding past T_c)
   constexpr uint32_t kLast = 0xffffffffu;   // NaN weights and padding: sorted last, E = 0
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + warp;
+  const int64_t row = (int64_t)blockIdx.x * kWarpRows<PER> + warp;
   if (row >= (int64_t)sh.B * sh.H * sh.T_r) return;
   const int i = (int)(row % sh.T_r);
   const int Tc = sh.T_c;
   int k_lo, k_hi;
   key_tile_range(sh, i, k_lo, k_hi);
   const float* wrow = logw + row * (int64_t)Tc;
-  uint32_t orig[8], key[8];
+  // the unsorted key of entry e: kept in registers up to PER = 16, re-read
+  // (from L1) above, so that more warps fit on an SM
+  constexpr bool kKeep = PER <= 16;
+  uint32_t orig[kKeep ? PER : 1], key[PER];
+  auto load_key = [&](int e) -> uint32_t {
+    const int m = lane * PER + e;
+    if (m >= Tc) return kLast;
+    const float dv = wrow[m];
+    return isnan(dv) ? kLast : order_key(dv);
+  };
+  auto unsorted = [&](int e) -> uint32_t {
+    if constexpr (kKeep) return orig[e];
+    else return load_key(e);
+  };
   int local_nan = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int m = lane * 8 + e;
-    orig[e] = kLast;
-    if (m < Tc) {
-      const float dv = wrow[m];
-      if (isnan(dv))
-        ++local_nan;
-      else
-        orig[e] = order_key(dv);
-    }
-    key[e] = orig[e];
+  for (int e = 0; e < PER; ++e) {
+    const int m = lane * PER + e;
+    key[e] = load_key(e);
+    if (m < Tc && key[e] == kLast) ++local_nan;
+    if constexpr (kKeep) orig[e] = key[e];
   }
   if (nan_count) {
     local_nan = __reduce_add_sync(0xffffffffu, local_nan);
     if (lane == 0 && local_nan) atomicAdd(nan_count, local_nan);
   }
 #pragma unroll
-  for (int kk = 2; kk <= 256; kk <<= 1) {
+  for (int kk = 2; kk <= N; kk <<= 1) {
 #pragma unroll
     for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      if (jj < 8) {
+      if (jj < PER) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < PER; ++e) {
           if (e & jj) continue;
-          const bool up = ((lane * 8 + e) & kk) == 0;
+          const bool up = ((lane * PER + e) & kk) == 0;
           const uint32_t lo = min(key[e], key[e | jj]), hi = max(key[e], key[e | jj]);
           key[e] = up ? lo : hi;
           key[e | jj] = up ? hi : lo;
         }
       } else {
-        const int lj = jj >> 3;
+        const int lj = jj / PER;
         const bool lower = (lane & lj) == 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < PER; ++e) {
           const uint32_t pk = __shfl_xor_sync(0xffffffffu, key[e], lj);
-          const bool up = ((lane * 8 + e) & kk) == 0;
+          const bool up = ((lane * PER + e) & kk) == 0;
           // the lower element of an ascending pair keeps the smaller key
           key[e] = (lower == up) ? min(key[e], pk) : max(key[e], pk);
         }
@@ -365,12 +387,10 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
   }
   // inclusive prefix of E in sorted order: nskip = the non-NaN positions whose
   // prefix stays below T (a prefix of the order)
-  unsigned long long E[8], tot = 0ull;
+  unsigned long long tot = 0ull;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    E[e] = key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
-    tot += E[e];
-  }
+  for (int e = 0; e < PER; ++e)
+    tot += key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
   unsigned long long incl = tot;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -380,8 +400,8 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
   unsigned long long pre = incl - tot;
   int nskip = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    pre += E[e];
+  for (int e = 0; e < PER; ++e) {
+    pre += key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
     nskip += (key[e] != kLast && pre < T);
   }
   nskip = __reduce_add_sync(0xffffffffu, nskip);
@@ -390,20 +410,16 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
   int r = 0;
   if (nskip > 0) {
     const int p = nskip - 1;
-    const int pe = p & 7;   // a select tree keeps key[] in registers
-    const uint32_t mine =
-        pe < 4 ? (pe < 2 ? (pe == 0 ? key[0] : key[1]) : (pe == 2 ? key[2] : key[3]))
-               : (pe < 6 ? (pe == 4 ? key[4] : key[5]) : (pe == 6 ? key[6] : key[7]));
-    kstar = __shfl_sync(0xffffffffu, mine, p >> 3);
+    kstar = __shfl_sync(0xffffffffu, pick<0, PER>(key, p % PER), p / PER);
     int less = 0;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) less += orig[e] < kstar;
+    for (int e = 0; e < PER; ++e) less += unsorted(e) < kstar;
     r = nskip - __reduce_add_sync(0xffffffffu, less);
   }
   // rank of each tie (key == K*) by j: warp exclusive scan of the per-lane counts
   int ties = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) ties += (nskip > 0 && orig[e] == kstar);
+  for (int e = 0; e < PER; ++e) ties += (nskip > 0 && unsorted(e) == kstar);
   int tie_off = ties;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -412,22 +428,23 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
   }
   tie_off -= ties;
   // the mask row and the ascending kv list
-  uint32_t fbits = 0u;   // bit e: entry 8 lane + e is kept
+  uint64_t fbits = 0ull;   // bit e: entry PER lane + e is kept
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int m = lane * 8 + e;
+  for (int e = 0; e < PER; ++e) {
+    const int m = lane * PER + e;
     bool skip = false;
     if (nskip > 0) {
-      if (orig[e] < kstar) {
+      const uint32_t ke = unsorted(e);
+      if (ke < kstar) {
         skip = true;
-      } else if (orig[e] == kstar) {
+      } else if (ke == kstar) {
         skip = tie_off < r;
         ++tie_off;
       }
     }
-    if (m < Tc && !skip && m >= k_lo && m <= k_hi) fbits |= 1u << e;
+    if (m < Tc && !skip && m >= k_lo && m <= k_hi) fbits |= 1ull << e;
   }
-  const int mine = __popc(fbits);
+  const int mine = __popcll(fbits);
   uint8_t* mrow = mask + row * (int64_t)Tc;
   int32_t* krow = kv_idx + row * (int64_t)Tc;
   int off = mine;
@@ -439,9 +456,9 @@ __global__ void __launch_bounds__(256) mask_rows_warp_kernel(
   const int cnt = __shfl_sync(0xffffffffu, off, 31);
   off -= mine;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int m = lane * 8 + e;
-    const uint32_t fe = (fbits >> e) & 1u;
+  for (int e = 0; e < PER; ++e) {
+    const int m = lane * PER + e;
+    const uint32_t fe = (uint32_t)(fbits >> e) & 1u;
     if (m < Tc) mrow[m] = (uint8_t)fe;
     if (fe) krow[off++] = m;
   }
@@ -479,30 +496,34 @@ cudaError_t launch_mask(const Shape& sh, const float* stats, const float* lse,
                         int32_t* nan_count, cudaStream_t st) {
   if (sh.T_c > kMaxTc) return cudaErrorInvalidValue;
   dim3 g1(sh.T_r, sh.H, sh.B);
-  auto rows = [&](auto rpl, auto cap) {
-    if (stats)
-      mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value, false>
-          <<<g1, kMaskThreads, 0, st>>>(stats, lse, nullptr, sh, threshold, mask, kv_idx, kv_cnt,
-                                        nan_count);
-    else if (decltype(cap)::value == 256) {
-      const int64_t rows_all = (int64_t)sh.B * sh.H * sh.T_r;
-      mask_rows_warp_kernel<<<(unsigned)((rows_all + 7) / 8), 256, 0, st>>>(
+  if (!stats) {   // from the tile weights: one warp per query tile
+    auto warp_rows = [&](auto per) {
+      constexpr int R = kWarpRows<decltype(per)::value>;
+      const unsigned blocks = (unsigned)(((int64_t)sh.B * sh.H * sh.T_r + R - 1) / R);
+      mask_rows_warp_kernel<decltype(per)::value><<<blocks, 32 * R, 0, st>>>(
           logw, sh, threshold, mask, kv_idx, kv_cnt, nan_count);
-    } else
-      mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value, true>
-          <<<g1, kMaskThreads, 0, st>>>(nullptr, nullptr, logw, sh, threshold, mask, kv_idx,
-                                        kv_cnt, nan_count);
-  };
-  auto by_cap = [&](auto rpl) {
-    if (sh.T_c <= 256) rows(rpl, std::integral_constant<int, 256>{});
-    else if (sh.T_c <= 512) rows(rpl, std::integral_constant<int, 512>{});
-    else if (sh.T_c <= 1024) rows(rpl, std::integral_constant<int, 1024>{});
-    else rows(rpl, std::integral_constant<int, 2048>{});
-  };
-  if (sh.block_q == 128)
-    by_cap(std::integral_constant<int, 4>{});
-  else
-    by_cap(std::integral_constant<int, 2>{});
+    };
+    if (sh.T_c <= 256) warp_rows(std::integral_constant<int, 8>{});
+    else if (sh.T_c <= 512) warp_rows(std::integral_constant<int, 16>{});
+    else if (sh.T_c <= 1024) warp_rows(std::integral_constant<int, 32>{});
+    else warp_rows(std::integral_constant<int, 64>{});
+  } else {
+    auto rows = [&](auto rpl, auto cap) {
+      mask_rows_kernel<decltype(rpl)::value, decltype(cap)::value>
+          <<<g1, kMaskThreads, 0, st>>>(stats, lse, sh, threshold, mask, kv_idx, kv_cnt,
+                                        nan_count);
+    };
+    auto by_cap = [&](auto rpl) {
+      if (sh.T_c <= 256) rows(rpl, std::integral_constant<int, 256>{});
+      else if (sh.T_c <= 512) rows(rpl, std::integral_constant<int, 512>{});
+      else if (sh.T_c <= 1024) rows(rpl, std::integral_constant<int, 1024>{});
+      else rows(rpl, std::integral_constant<int, 2048>{});
+    };
+    if (sh.block_q == 128)
+      by_cap(std::integral_constant<int, 4>{});
+    else
+      by_cap(std::integral_constant<int, 2>{});
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2((sh.T_c + 7) / 8, sh.H, sh.B);

@@ -96,11 +96,12 @@ def test_tile_weights_match_the_oracle_and_the_stats_path(w):
         U.assert_lists_equal(a, ref_lists)
 
 
-@pytest.mark.parametrize("n", [1024, 640, 32768, 38400])
+@pytest.mark.parametrize("n", [1024, 640, 32768, 38400, 128000, 262144])
 def test_tile_weights_mask_on_planted_weights(n):
     """Hand-built weights with ties, -inf and NaN tiles: the mask from the
-    weights is the oracle's selection of exactly those rows.  T_c = 8, 5 and
-    256 run the one-warp-per-row kernel, T_c = 300 the block-per-row one."""
+    weights is the oracle's selection of exactly those rows.  T_c = 5, 8,
+    256, 300, 1000 and 2048 run the one-warp-per-row kernel with 8, 16, 32
+    and 64 entries per lane."""
     from block_sparse_attention_fwd_gb300 import _lib
     B, H = 1, 2
     shape = _lib.make_shape(B, n, H, H, 128, 128, 128)
