@@ -29,23 +29,23 @@
 //                       columns [0,32) and [64,96), the TMEM A operand of
 //                       dK += dS^T Q; then the dQ tile dS K (issued after dK)
 //   dV   [256,256+d)    dK [256+d,256+2d)
-// Per tile the issuer queues dV as soon as the softmax has written P^T
-// (first phase) and the next tile's S^T right behind it, so S^T runs while
-// the softmax forms dS^T (second phase); then dK and dQ once dS^T is in
-// shared memory, and the next tile's dP^T once the dQ tile has been drained
-// from R_dP.  The tensor core runs them in issue order, which makes every
-// reuse safe: S^T of the next tile (into R_S) is queued behind dV, which
-// reads P^T from R_S, and dS^T is rewritten only after the next dP^T, hence
-// after dK and dQ, have completed.  The first dV and dK of an item overwrite
-// the accumulators: they are issued after the softmax warps, which read the
-// previous item's accumulators in their epilogue, have signalled the item's
-// first tile.
+// The issuer queues, per tile t: dK_t and dQ_t once the softmax has put
+// dS^T_t in shared memory (second phase); then, for the next tile, dV_{t+1}
+// once the first phase has written P^T_{t+1}, which runs while the drain
+// empties R_dP of dQ_t; dP^T_{t+1} once R_dP is drained; and S^T_{t+2}
+// right behind it, which runs while the softmax forms dS^T_{t+1}.  The
+// tensor core runs them in issue order, which makes every reuse safe: S^T
+// (into R_S) is queued behind the dV that reads P^T from R_S, and dS^T is
+// rewritten only after the next dP^T, hence after dK and dQ, have completed.
+// The first dV and dK of an item overwrite the accumulators: they are issued
+// after the softmax warps, which read the previous item's accumulators in
+// their epilogue, have signalled the item's first tile.
 // Warp roles (16 warps):
 //   warp 0      TMA producer: per item K_j, V_j; per tile Q_i into two
 //               alternating slots and dO_i into a third (4-D tensor maps,
 //               128-byte swizzle, rows past n read as 0), plus the tile's
-//               LSE and D rows; dO's slot frees once dV has read it, so the
-//               next dO loads while dK, S^T and dQ run.
+//               LSE and D rows; dO's slot frees once dV and dP^T have read
+//               it, so the next dO loads while S^T, dK and dQ run.
 //   warp 1      MMA issuer (one thread) and TMEM owner.
 //   warps 2-3   take the next item from the global counter and copy its
 //               tile lists into one of two shared-memory list buffers, one
@@ -120,8 +120,8 @@ struct Bars {
 
 // Load x = 2t brings Q_t, x = 2t + 1 brings dO_t.  Q_t alternates between
 // slots 0 and 1 (its last reader, dK_t, frees it); every dO uses slot 2,
-// which frees as soon as dV_t (its last reader) completes, so the next dO
-// loads while dK_t, S^T and dQ run.
+// which frees as soon as dP^T_t (its last reader) completes, so the next dO
+// loads while S^T, dK_t and dQ_t run.
 __device__ __forceinline__ int slot_of(int x) { return (x & 1) ? 2 : ((x >> 1) & 1); }
 __device__ __forceinline__ uint32_t phase_of(int x) {
   return (uint32_t)(((x & 1) ? (x >> 1) : (x >> 2)) & 1);
@@ -414,44 +414,49 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         if (m < 0) break;
         const Item it = item_of(sh, m);
         Walk<SUB> walk = make_walk(it, buf);
+        // dV_u = P^T dO_u (P^T from TMEM); the item's first one overwrites
+        auto issue_dv = [&](int u, bool fst) {
+          const uint64_t gmn = sdesc_sw128(slot_addr(2 * u + 1), C::CHUNK, 1024);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t pcol = C::T_S + (ks >> 2) * 64 + (ks & 3) * 8;
+            mma_ts(tmem + C::T_DV, tmem + pcol, gmn + ks * (2048 >> 4), C::ID_G,
+                   (!fst || ks > 0) ? 1u : 0u);
+          }
+        };
         bool have = step(walk, buf);
+        bool next = false;
         if (have) {
-          // the item's first tile: S^T needs its K, dP^T its V and a drained R_dP
+          // the item's first tile: S^T needs its K; dV the first softmax phase;
+          // dP^T its V and a drained R_dP
           ok = wait_phase<WL>(&bars.kv_full, kk & 1, &s_wait) && wait_slot(2 * t);
           if (!ok) break;
           fence_after_sync();
           issue_s(t);
-          ok = (t == 0 || wait_phase<WL>(&bars.dq_free, (t - 1) & 1, &s_wait)) && wait_slot(2 * t + 1);
+          ok = !failed(&s_fail) && wait_phase<WL>(&bars.p1_ready, t & 1, &s_wait) &&
+               wait_slot(2 * t + 1);
+          if (!ok) break;
+          fence_after_sync();
+          issue_dv(t, true);
+          ok = t == 0 || wait_phase<WL>(&bars.dq_free, (t - 1) & 1, &s_wait);
           if (!ok) break;
           fence_after_sync();
           issue_dp(t);
-        }
-        bool first = true;
-        while (ok && have) {
-          // dV_t as soon as the first softmax phase has written P^T; it runs
-          // while the second phase forms dS^T
-          ok = !failed(&s_fail) && wait_phase<WL>(&bars.p1_ready, t & 1, &s_wait);
-          if (!ok) break;
-          fence_after_sync();
-          const uint64_t gmn = sdesc_sw128(slot_addr(2 * t + 1), C::CHUNK, 1024);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {      // dV += P^T dO  (P^T from TMEM)
-            const uint32_t pcol = C::T_S + (ks >> 2) * 64 + (ks & 3) * 8;
-            mma_ts(tmem + C::T_DV, tmem + pcol, gmn + ks * (2048 >> 4), C::ID_G,
-                   (!first || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars.empty[2]);           // dO_t's slot: dP^T and dV have read it
-          // S^T of the next tile of this item right behind dV (which read P^T
-          // from R_S): it runs while the softmax forms dS^T
-          const bool next = step(walk, buf);
+          mma_commit(&bars.empty[2]);           // dO_t's slot: dV and dP^T have read it
+          // S^T of the next tile right behind dP^T: it runs while the softmax
+          // forms dS^T
+          next = step(walk, buf);
           if (next) {
             ok = wait_slot(2 * (t + 1));
             if (!ok) break;
             fence_after_sync();
             issue_s(t + 1);
           }
-          // dK_t once dS^T is in shared memory
-          ok = wait_phase<WL>(&bars.p2_ready, t & 1, &s_wait);
+        }
+        bool first = true;
+        while (ok && have) {
+          // dK_t and dQ_t once dS^T is in shared memory
+          ok = !failed(&s_fail) && wait_phase<WL>(&bars.p2_ready, t & 1, &s_wait);
           if (!ok) break;
           fence_after_sync();
           const uint32_t dsb = opaque(sDS);
@@ -473,16 +478,32 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
                    ks > 0 ? 1u : 0u);
           mma_commit(&bars.dq_ready);
           if (!next) mma_commit(&bars.kv_empty);  // K and V of this item are read
+          bool next2 = false;
           if (next) {
-            // dP^T of the next tile once the dQ tile has left R_dP; the dS^T
-            // buffer is rewritten only after dP^T completes, hence after dQ
-            ok = wait_phase<WL>(&bars.dq_free, t & 1, &s_wait) && wait_slot(2 * (t + 1) + 1);
+            // dV of the next tile runs while the drain empties R_dP; then its
+            // dP^T.  The dS^T buffer is rewritten only after that dP^T
+            // completes, hence after dQ_t.
+            ok = wait_phase<WL>(&bars.p1_ready, (t + 1) & 1, &s_wait) &&
+                 wait_slot(2 * (t + 1) + 1);
+            if (!ok) break;
+            fence_after_sync();
+            issue_dv(t + 1, false);
+            ok = wait_phase<WL>(&bars.dq_free, t & 1, &s_wait);
             if (!ok) break;
             fence_after_sync();
             issue_dp(t + 1);
+            mma_commit(&bars.empty[2]);         // dO_{t+1}'s slot
+            next2 = step(walk, buf);
+            if (next2) {
+              ok = wait_slot(2 * (t + 2));
+              if (!ok) break;
+              fence_after_sync();
+              issue_s(t + 2);
+            }
           }
           first = false;
           have = next;
+          next = next2;
           ++t;
         }
         if (!ok) break;
