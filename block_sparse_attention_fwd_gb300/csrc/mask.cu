@@ -317,6 +317,8 @@ __device__ __forceinline__ uint32_t pick(const uint32_t* k, int idx) {
 // many registers, so that more of them fit on an SM
 template <int PER>
 constexpr int kWarpRows = PER <= 8 ? 8 : 2;
+// rows that keep more tiles than this are sorted
+constexpr int kMaxTop = 32;
 
 template <int PER>
 __global__ void __launch_bounds__(32 * kWarpRows<PER>) mask_rows_warp_kernel(
@@ -359,90 +361,150 @@ __global__ void __launch_bounds__(32 * kWarpRows<PER>) mask_rows_warp_kernel(
     local_nan = __reduce_add_sync(0xffffffffu, local_nan);
     if (lane == 0 && local_nan) atomicAdd(nan_count, local_nan);
   }
+  uint64_t fbits = 0ull;   // bit e: entry PER lane + e is kept (mask row)
+  // Few kept tiles, the usual case: the kept entries are the top K in (d
+  // desc, j desc) order, K the least count whose removal leaves a sum of E
+  // below T -- the complement of the longest prefix in (d asc, j asc) order
+  // whose sum stays below T.  They are taken one at a time with a warp-wide
+  // max of (key, j); a row that keeps more than kMaxTop is sorted instead.
+  // At 8 entries per lane the sort is cheaper than the extraction and always
+  // runs.
+  bool sort_row = true;
+  if constexpr (PER > 8) {
+    unsigned long long S = 0ull;
+    int nn = 0;
 #pragma unroll
-  for (int kk = 2; kk <= N; kk <<= 1) {
+    for (int e = 0; e < PER; ++e)
+      if (key[e] != kLast) {
+        S += detexp_fixed40(key_to_d(key[e]));
+        ++nn;
+      }
 #pragma unroll
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      if (jj < PER) {
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    nn = __reduce_add_sync(0xffffffffu, nn);
+    uint64_t kept = 0ull;
+    auto lane_best = [&]() {   // 0: none (every valid (key, j) is above 0)
+      unsigned long long bst = 0ull;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
-          if (e & jj) continue;
-          const bool up = ((lane * PER + e) & kk) == 0;
-          const uint32_t lo = min(key[e], key[e | jj]), hi = max(key[e], key[e | jj]);
-          key[e] = up ? lo : hi;
-          key[e | jj] = up ? hi : lo;
-        }
-      } else {
-        const int lj = jj / PER;
-        const bool lower = (lane & lj) == 0;
+      for (int e = 0; e < PER; ++e)
+        if (!((kept >> e) & 1ull) && key[e] != kLast)
+          bst = max(bst, ((unsigned long long)key[e] << 32) | (unsigned)(lane * PER + e));
+      return bst;
+    };
+    unsigned long long best = lane_best(), taken = 0ull;
+    for (int k = 0;; ++k) {
+      if (k >= nn || S - taken < T) {
+        sort_row = false;
+        break;
+      }
+      if (k >= kMaxTop) break;
+      unsigned long long w = best;
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
-          const uint32_t pk = __shfl_xor_sync(0xffffffffu, key[e], lj);
-          const bool up = ((lane * PER + e) & kk) == 0;
-          // the lower element of an ascending pair keeps the smaller key
-          key[e] = (lower == up) ? min(key[e], pk) : max(key[e], pk);
-        }
+      for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
+      const int j = (int)(w & 0xffffffffull), owner = j / PER;
+      unsigned long long ew = 0ull;
+      if (lane == owner) {
+        kept |= 1ull << (j - lane * PER);
+        ew = detexp_fixed40(key_to_d((uint32_t)(w >> 32)));
+        best = lane_best();
+      }
+      taken += __shfl_sync(0xffffffffu, ew, owner);
+    }
+    if (!sort_row) {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        const int m = lane * PER + e;
+        // NaN weights are never skipped
+        if (m < Tc && (key[e] == kLast || ((kept >> e) & 1ull)) && m >= k_lo && m <= k_hi)
+          fbits |= 1ull << e;
       }
     }
   }
-  // inclusive prefix of E in sorted order: nskip = the non-NaN positions whose
-  // prefix stays below T (a prefix of the order)
-  unsigned long long tot = 0ull;
-#pragma unroll
-  for (int e = 0; e < PER; ++e)
-    tot += key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
-  unsigned long long incl = tot;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
-  }
-  unsigned long long pre = incl - tot;
-  int nskip = 0;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    pre += key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
-    nskip += (key[e] != kLast && pre < T);
-  }
-  nskip = __reduce_add_sync(0xffffffffu, nskip);
-  // K*: the sorted key at position nskip - 1; r of its ties are skipped
-  uint32_t kstar = 0u;
-  int r = 0;
-  if (nskip > 0) {
-    const int p = nskip - 1;
-    kstar = __shfl_sync(0xffffffffu, pick<0, PER>(key, p % PER), p / PER);
-    int less = 0;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) less += unsorted(e) < kstar;
-    r = nskip - __reduce_add_sync(0xffffffffu, less);
-  }
-  // rank of each tie (key == K*) by j: warp exclusive scan of the per-lane counts
-  int ties = 0;
-#pragma unroll
-  for (int e = 0; e < PER; ++e) ties += (nskip > 0 && unsorted(e) == kstar);
-  int tie_off = ties;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, tie_off, o);
-    if (lane >= o) tie_off += y;
-  }
-  tie_off -= ties;
-  // the mask row and the ascending kv list
-  uint64_t fbits = 0ull;   // bit e: entry PER lane + e is kept
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int m = lane * PER + e;
-    bool skip = false;
+  if (sort_row) {
+  #pragma unroll
+    for (int kk = 2; kk <= N; kk <<= 1) {
+  #pragma unroll
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        if (jj < PER) {
+  #pragma unroll
+          for (int e = 0; e < PER; ++e) {
+            if (e & jj) continue;
+            const bool up = ((lane * PER + e) & kk) == 0;
+            const uint32_t lo = min(key[e], key[e | jj]), hi = max(key[e], key[e | jj]);
+            key[e] = up ? lo : hi;
+            key[e | jj] = up ? hi : lo;
+          }
+        } else {
+          const int lj = jj / PER;
+          const bool lower = (lane & lj) == 0;
+  #pragma unroll
+          for (int e = 0; e < PER; ++e) {
+            const uint32_t pk = __shfl_xor_sync(0xffffffffu, key[e], lj);
+            const bool up = ((lane * PER + e) & kk) == 0;
+            // the lower element of an ascending pair keeps the smaller key
+            key[e] = (lower == up) ? min(key[e], pk) : max(key[e], pk);
+          }
+        }
+      }
+    }
+    // inclusive prefix of E in sorted order: nskip = the non-NaN positions whose
+    // prefix stays below T (a prefix of the order)
+    unsigned long long tot = 0ull;
+  #pragma unroll
+    for (int e = 0; e < PER; ++e)
+      tot += key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
+    unsigned long long incl = tot;
+  #pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    unsigned long long pre = incl - tot;
+    int nskip = 0;
+  #pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      pre += key[e] != kLast ? detexp_fixed40(key_to_d(key[e])) : 0ull;
+      nskip += (key[e] != kLast && pre < T);
+    }
+    nskip = __reduce_add_sync(0xffffffffu, nskip);
+    // K*: the sorted key at position nskip - 1; r of its ties are skipped
+    uint32_t kstar = 0u;
+    int r = 0;
     if (nskip > 0) {
-      const uint32_t ke = unsorted(e);
-      if (ke < kstar) {
-        skip = true;
-      } else if (ke == kstar) {
-        skip = tie_off < r;
-        ++tie_off;
-      }
+      const int p = nskip - 1;
+      kstar = __shfl_sync(0xffffffffu, pick<0, PER>(key, p % PER), p / PER);
+      int less = 0;
+  #pragma unroll
+      for (int e = 0; e < PER; ++e) less += unsorted(e) < kstar;
+      r = nskip - __reduce_add_sync(0xffffffffu, less);
     }
-    if (m < Tc && !skip && m >= k_lo && m <= k_hi) fbits |= 1ull << e;
+    // rank of each tie (key == K*) by j: warp exclusive scan of the per-lane counts
+    int ties = 0;
+  #pragma unroll
+    for (int e = 0; e < PER; ++e) ties += (nskip > 0 && unsorted(e) == kstar);
+    int tie_off = ties;
+  #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, tie_off, o);
+      if (lane >= o) tie_off += y;
+    }
+    tie_off -= ties;
+    // the mask row
+  #pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int m = lane * PER + e;
+      bool skip = false;
+      if (nskip > 0) {
+        const uint32_t ke = unsorted(e);
+        if (ke < kstar) {
+          skip = true;
+        } else if (ke == kstar) {
+          skip = tie_off < r;
+          ++tie_off;
+        }
+      }
+      if (m < Tc && !skip && m >= k_lo && m <= k_hi) fbits |= 1ull << e;
+    }
   }
   const int mine = __popcll(fbits);
   uint8_t* mrow = mask + row * (int64_t)Tc;
