@@ -26,6 +26,12 @@ CASES = [
     (inputs.custom("ragged_n300_d128_t128", B=1, n=300, H=3, Hk=1, d=128, run=16,
                    clusters=4, alpha=2.0), 0.02),
     (inputs.WORKLOADS["clustered_n4096_d64"], 0.05),
+    # degenerate shapes: one partial tile per sequence (three sequences), and
+    # one full plus one single-row tile
+    (inputs.custom("edge_n100_d128_b3", B=3, n=100, H=2, Hk=1, d=128, run=16, clusters=3,
+                   alpha=2.0), 0.05),
+    (inputs.custom("edge_n65_d64_t64", B=1, n=65, H=1, Hk=1, d=64, block_q=64, block_k=64,
+                   run=8, clusters=3, alpha=2.0), 0.3),
 ]
 
 
