@@ -23,7 +23,9 @@ EXPORTS = ("bl_tile_stats_elems", "bl_lists_elems", "bl_bwd_workspace_bytes", "b
            "bl_mask_from_stats", "bl_fwd_workspace_bytes", "bl_attn_fwd_tile_weights",
            "bl_mask_from_tile_weights", "bl_attn_bwd", "bl_bwd_check_status", "bl_status_string",
            "bl_attn_bwd_noalloc", "bl_bwd_noalloc_check_status", "bl_lse_combine", "bl_grad_error", "bl_varlen_layout",
-           "bl_attn_fwd_varlen", "bl_mask_from_stats_varlen", "bl_attn_bwd_varlen",
+           "bl_attn_fwd_varlen", "bl_mask_from_stats_varlen", "bl_fwd_workspace_bytes_varlen",
+           "bl_attn_fwd_tile_weights_varlen", "bl_mask_from_tile_weights_varlen",
+           "bl_attn_bwd_varlen",
            "bl_varlen_bwd_check_status", "bl_set_wait_limit")
 
 
@@ -117,6 +119,12 @@ def load():
     lib.bl_attn_fwd_varlen.restype = ctypes.c_int
     lib.bl_mask_from_stats_varlen.argtypes = [V, P, P, D, ctypes.POINTER(Lists), P]
     lib.bl_mask_from_stats_varlen.restype = ctypes.c_int
+    lib.bl_fwd_workspace_bytes_varlen.argtypes = [V]
+    lib.bl_fwd_workspace_bytes_varlen.restype = ctypes.c_size_t
+    lib.bl_attn_fwd_tile_weights_varlen.argtypes = [V, P, P, P, F, P, P, P, P, P, Z, P]
+    lib.bl_attn_fwd_tile_weights_varlen.restype = ctypes.c_int
+    lib.bl_mask_from_tile_weights_varlen.argtypes = [V, P, D, ctypes.POINTER(Lists), P]
+    lib.bl_mask_from_tile_weights_varlen.restype = ctypes.c_int
     lib.bl_attn_bwd_varlen.argtypes = [V, P, P, P, P, P, P, F, ctypes.POINTER(Lists), P, P, P,
                                        P, Z, P]
     lib.bl_attn_bwd_varlen.restype = ctypes.c_int
@@ -473,6 +481,58 @@ def mask_from_stats_varlen(vl: Varlen, tile_stats, lse, negl_prob, lists):
                                             _ptr(lse), float(negl_prob), ctypes.byref(ls),
                                             _stream(lse.device))
     _check("bl_mask_from_stats_varlen", code)
+
+
+def fwd_tile_weights_supported_varlen(vl: Varlen) -> bool:
+    """Whether bl_attn_fwd_tile_weights_varlen takes this batch (128 x 128
+    tiles, head dim 64 or 128, at most 2048 key tiles per sequence)."""
+    longest = max(b - a for a, b in zip(vl.cu_seqlens[:-1], vl.cu_seqlens[1:]))
+    return (vl.block_q == 128 and vl.block_k == 128 and vl.d in (64, 128)
+            and -(-longest // 128) <= 2048)
+
+
+def fwd_workspace_bytes_varlen(vl: Varlen) -> int:
+    """Scratch of attn_fwd_tile_weights_varlen without a statistics output."""
+    return int(load().bl_fwd_workspace_bytes_varlen(ctypes.byref(vl.struct)))
+
+
+def attn_fwd_tile_weights_varlen(vl: Varlen, q, k, v, scale, o, lse, tile_logw, tile_stats=None,
+                                 workspace=None):
+    """bl_attn_fwd_tile_weights_varlen: tile_logw holds sizes["mask"] floats,
+    laid out like the mask."""
+    T, H, Hk, d = vl.total, vl.H, vl.Hk, vl.d
+    _need(q, torch.bfloat16, (T, H, d), "q")
+    _need(k, torch.bfloat16, (T, Hk, d), "k")
+    _need(v, torch.bfloat16, (T, Hk, d), "v")
+    _need(o, torch.bfloat16, (T, H, d), "o")
+    _need(lse, torch.float32, (vl.sizes["lse"],), "lse")
+    _need(tile_logw, torch.float32, (vl.sizes["mask"],), "tile_logw")
+    if tile_stats is not None:
+        _need(tile_stats, torch.float32, (vl.sizes["tile_stats"],), "tile_stats")
+    nbytes = 0
+    if workspace is not None:
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+            raise TypeError("workspace must be a CUDA uint8 tensor")
+        nbytes = workspace.numel()
+    code = load().bl_attn_fwd_tile_weights_varlen(
+        ctypes.byref(vl.struct), _ptr(q), _ptr(k), _ptr(v), float(scale), _ptr(o), _ptr(lse),
+        _ptr(tile_stats), _ptr(tile_logw), _ptr(workspace), nbytes, _stream(q.device))
+    _check("bl_attn_fwd_tile_weights_varlen", code)
+
+
+def mask_from_tile_weights_varlen(vl: Varlen, tile_logw, negl_prob, lists):
+    z = vl.sizes
+    _need(tile_logw, torch.float32, (z["mask"],), "tile_logw")
+    _need(lists["mask"], torch.uint8, (z["mask"],), "mask")
+    _need(lists["kv_idx"], torch.int32, (z["mask"],), "kv_idx")
+    _need(lists["kv_cnt"], torch.int32, (z["kv_cnt"],), "kv_cnt")
+    _need(lists["q_idx"], torch.int32, (z["q_idx"],), "q_idx")
+    _need(lists["q_cnt"], torch.int32, (z["q_cnt"],), "q_cnt")
+    ls = _lists_struct(lists)
+    code = load().bl_mask_from_tile_weights_varlen(ctypes.byref(vl.struct), _ptr(tile_logw),
+                                                   float(negl_prob), ctypes.byref(ls),
+                                                   _stream(tile_logw.device))
+    _check("bl_mask_from_tile_weights_varlen", code)
 
 
 def attn_bwd_varlen(vl: Varlen, q, k, v, o, g_o, lse, scale, lists, g_q, g_k, g_v, workspace):

@@ -96,12 +96,19 @@ class _BLAttnVarlenFn(torch.autograd.Function):
     def forward(ctx, q, k, v, vl, scale, negl_prob):
         o = torch.empty_like(q)
         lse = torch.empty(vl.sizes["lse"], dtype=torch.float32, device=q.device)
-        stats = None
-        if negl_prob > 0:
-            stats = torch.empty(vl.sizes["tile_stats"], dtype=torch.float32, device=q.device)
-        _lib.attn_fwd_varlen(vl, q, k, v, scale, o, lse, stats)
+        stats = logw = None
+        if negl_prob > 0 and _lib.fwd_tile_weights_supported_varlen(vl):
+            logw = torch.empty(vl.sizes["mask"], dtype=torch.float32, device=q.device)
+            ws = torch.empty(_lib.fwd_workspace_bytes_varlen(vl), dtype=torch.uint8,
+                             device=q.device)
+            _lib.attn_fwd_tile_weights_varlen(vl, q, k, v, scale, o, lse, logw, workspace=ws)
+        else:
+            if negl_prob > 0:
+                stats = torch.empty(vl.sizes["tile_stats"], dtype=torch.float32,
+                                    device=q.device)
+            _lib.attn_fwd_varlen(vl, q, k, v, scale, o, lse, stats)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.stats = stats
+        ctx.stats, ctx.logw = stats, logw
         ctx.cfg = (vl, scale, negl_prob)
         ctx.mark_non_differentiable(lse)
         return o, lse
@@ -111,9 +118,12 @@ class _BLAttnVarlenFn(torch.autograd.Function):
         q, k, v, o, lse = ctx.saved_tensors
         vl, scale, negl_prob = ctx.cfg
         lists = None
-        if ctx.stats is not None:
+        if ctx.stats is not None or ctx.logw is not None:
             lists = _lib.alloc_varlen_lists(vl, q.device)
-            _lib.mask_from_stats_varlen(vl, ctx.stats, lse, negl_prob, lists)
+            if ctx.logw is not None:
+                _lib.mask_from_tile_weights_varlen(vl, ctx.logw, negl_prob, lists)
+            else:
+                _lib.mask_from_stats_varlen(vl, ctx.stats, lse, negl_prob, lists)
         g_q, g_k, g_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(vl.sizes["bwd_workspace_bytes"], dtype=torch.uint8, device=q.device)
         _lib.attn_bwd_varlen(vl, q, k, v, o, g_o.contiguous(), lse, scale, lists, g_q, g_k, g_v,

@@ -83,12 +83,15 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 // Scratch for the tile weights without a statistics output: `nslots` slots
 // of [T_c][kRowStride] floats (the two query tiles' 256 rows of every key
 // tile, then 4 floats of padding), one per CTA that can be resident at once,
-// each claimed with a lock word.
+// each claimed with a lock word.  Slots are slot_floats apart (T_c *
+// kRowStride for one call; the largest T_c when the launches of a packed
+// batch share the slots).
 constexpr int kRowStride = 260;
 struct RowScratch {
   float* slots;
   int32_t* locks;
   int nslots;
+  int64_t slot_floats;
 };
 
 // SUB: statistics per 128-key MMA tile (1 for 128-key tiles, 2 for 64-key
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       st_row = stats + bh * sh.T_c * sh.n_pad + row;
       st_stride = (int)sh.n_pad;
     } else if (s_slot >= 0) {
-      st_row = scr.slots + (int64_t)s_slot * sh.T_c * kRowStride + t * 128 + r;
+      st_row = scr.slots + (int64_t)s_slot * scr.slot_floats + t * 128 + r;
       st_stride = kRowStride;
     }
     float m_ref = -INFINITY, l_run = 0.f;
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       key_tile_range(sh, 2 * pair, lo0, hi0);
       if (ntile == 2) key_tile_range(sh, 2 * pair + 1, lo1, hi1);
       gsrc = stats ? stats + bh * sh.T_c * sh.n_pad + pair * 256
-                   : (s_slot >= 0 ? scr.slots + (int64_t)s_slot * Tc * kRowStride : nullptr);
+                   : (s_slot >= 0 ? scr.slots + (int64_t)s_slot * scr.slot_floats : nullptr);
       gstride = stats ? sh.n_pad : kRowStride;
       rowbytes = (stats && ntile == 1) ? 512u : 1024u;
       issuer = ww == 0 && lane == 0 && gsrc != nullptr;
@@ -581,7 +584,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
 template <int D, int SUB, bool WL>
 cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                      float* lse, float* stats, float* logw, RowScratch scr, float scale,
-                     cudaStream_t st) {
+                     bool zero_locks, cudaStream_t st) {
   using C = FCfg<D>;
   CUtensorMap mq, mk, mv;
   if (!make_bshd_map(&mq, q, sh.B, sh.n, sh.H, D, 128, sh.qs) ||
@@ -592,7 +595,7 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
   auto kern = fwd_tc_kernel<D, SUB, WL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (scr.locks) {
+  if (scr.locks && zero_locks) {
     e = cudaMemsetAsync(scr.locks, 0, (size_t)scr.nslots * sizeof(int32_t), st);
     if (e != cudaSuccess) return e;
   }
@@ -631,17 +634,25 @@ bool fwd_tile_weights_supported(const Shape& sh) {
          sh.T_c <= 2048;
 }
 
-size_t fwd_scratch_bytes(const Shape& sh) {
-  const int ns = sh.d == 128 ? resident_ctas<128>() : resident_ctas<64>();
+size_t fwd_scratch_bytes(int d, int T_c) {
+  const int ns = d == 128 ? resident_ctas<128>() : resident_ctas<64>();
   if (ns <= 0) return 0;
   const size_t locks = ((size_t)ns * sizeof(int32_t) + 255) & ~(size_t)255;
-  return locks + (size_t)ns * sh.T_c * kRowStride * sizeof(float);
+  return locks + (size_t)ns * T_c * kRowStride * sizeof(float);
+}
+
+size_t fwd_scratch_bytes(const Shape& sh) { return fwd_scratch_bytes(sh.d, sh.T_c); }
+
+cudaError_t fwd_scratch_clear(int d, void* scratch, cudaStream_t st) {
+  const int ns = d == 128 ? resident_ctas<128>() : resident_ctas<64>();
+  if (ns <= 0 || !scratch) return cudaErrorInvalidValue;
+  return cudaMemsetAsync(scratch, 0, (size_t)ns * sizeof(int32_t), st);
 }
 
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                           float* lse, float* stats, float* logw, void* scratch, float scale,
-                          cudaStream_t st) {
-  RowScratch scr{nullptr, nullptr, 0};
+                          cudaStream_t st, int slot_tc, bool zero_locks) {
+  RowScratch scr{nullptr, nullptr, 0, 0};
   if (logw && !stats) {
     const int ns = sh.d == 128 ? resident_ctas<128>() : resident_ctas<64>();
     if (ns <= 0 || !scratch) return cudaErrorInvalidValue;
@@ -649,11 +660,14 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
     scr.locks = static_cast<int32_t*>(scratch);
     scr.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + locks);
     scr.nslots = ns;
+    if (slot_tc <= 0) slot_tc = sh.T_c;
+    if (slot_tc < sh.T_c) return cudaErrorInvalidValue;
+    scr.slot_floats = (int64_t)slot_tc * kRowStride;
   }
   if (sh.block_k == 64 && logw) return cudaErrorInvalidValue;   // tile weights: 128 x 128 tiles
   auto go = [&](auto d_c, auto sub_c, auto wl_c) {
     return launch_t<decltype(d_c)::value, decltype(sub_c)::value, decltype(wl_c)::value>(
-        sh, q, k, v, o, lse, stats, logw, scr, scale, st);
+        sh, q, k, v, o, lse, stats, logw, scr, scale, zero_locks, st);
   };
   using I64 = std::integral_constant<int, 64>;
   using I128 = std::integral_constant<int, 128>;

@@ -50,9 +50,15 @@ cudaError_t launch_bwd_tc(const Shape& sh, const void* q, const void* k, const v
 bool fwd_tc_supported(const Shape& sh);
 bool fwd_tile_weights_supported(const Shape& sh);
 size_t fwd_scratch_bytes(const Shape& sh);
+size_t fwd_scratch_bytes(int d, int T_c);
+// Clears the slot locks of a forward scratch (the first bytes of it).
+cudaError_t fwd_scratch_clear(int d, void* scratch, cudaStream_t st);
+// slot_tc: key tiles a scratch slot holds (0: sh.T_c); zero_locks: clear the
+// slot locks on st first (launches that share a scratch clear it once, before
+// any of them).
 cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const void* v, void* o,
                           float* lse, float* stats, float* logw, void* scratch, float scale,
-                          cudaStream_t st);
+                          cudaStream_t st, int slot_tc = 0, bool zero_locks = true);
 
 // LSE-combine of `parts` partial results (layouts in include/bl_attn.h).
 // Error sums of bf16 a against bf16 b (n elements) into out[4] (fp64).

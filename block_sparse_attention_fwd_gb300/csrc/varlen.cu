@@ -264,6 +264,70 @@ bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_s
   });
 }
 
+size_t bl_fwd_workspace_bytes_varlen(const bl_varlen* varlen) {
+  Plan p;
+  if (make_plan(varlen, &p) != BL_OK) return 0;
+  for (const Run& r : p.runs)
+    if (!bl::fwd_tile_weights_supported(r.sh)) return 0;
+  return bl::fwd_scratch_bytes(varlen->d, p.max_T_c);
+}
+
+bl_status bl_attn_fwd_tile_weights_varlen(const bl_varlen* varlen, const void* q, const void* k,
+                                          const void* v, float scale, void* o, float* lse,
+                                          float* tile_stats, float* tile_logw, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  Plan p;
+  bl_status st = make_plan(varlen, &p);
+  if (st != BL_OK) return st;
+  if (!q || !k || !v || !o || !lse || !tile_logw) return BL_ERR_INVALID_ARG;
+  if (!bl::aligned16(q) || !bl::aligned16(k) || !bl::aligned16(v) || !bl::aligned16(o) ||
+      !aligned4(lse) || !aligned4(tile_logw) || (tile_stats && !bl::aligned16(tile_stats)))
+    return BL_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return BL_ERR_INVALID_ARG;
+  for (const Run& r : p.runs)
+    if (!bl::fwd_tile_weights_supported(r.sh)) return BL_ERR_UNSUPPORTED;
+  if (!tile_stats) {
+    const size_t need = bl::fwd_scratch_bytes(varlen->d, p.max_T_c);
+    if (need == 0) return BL_ERR_CUDA;
+    if (!workspace || !bl::aligned16(workspace) || workspace_bytes < need)
+      return BL_ERR_WORKSPACE;
+    // every launch group claims slots of the one scratch (sized for the
+    // longest sequence): its locks are cleared once, on the caller's stream
+    // before the groups fork
+    if (bl::fwd_scratch_clear(varlen->d, workspace, (cudaStream_t)stream) != cudaSuccess)
+      return BL_ERR_CUDA;
+  }
+  const int H = varlen->H, Hk = varlen->Hk, d = varlen->d;
+  return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
+    return bl::launch_fwd_tc(r.sh, rows(q, r.tok, H, d), rows(k, r.tok, Hk, d),
+                             rows(v, r.tok, Hk, d), rows(o, r.tok, H, d), lse + r.lse,
+                             at(tile_stats, r.stats), tile_logw + r.mask,
+                             tile_stats ? nullptr : workspace, scale, st, p.max_T_c,
+                             /*zero_locks=*/false);
+  });
+}
+
+bl_status bl_mask_from_tile_weights_varlen(const bl_varlen* varlen, const float* tile_logw,
+                                           double negl_prob, const bl_lists* lists,
+                                           void* stream) {
+  Plan p;
+  bl_status st = make_plan(varlen, &p);
+  if (st != BL_OK) return st;
+  if (!tile_logw || !lists) return BL_ERR_INVALID_ARG;
+  if (!lists->mask || !lists->kv_idx || !lists->kv_cnt || !lists->q_idx || !lists->q_cnt)
+    return BL_ERR_INVALID_ARG;
+  if (!aligned4(tile_logw)) return BL_ERR_INVALID_ARG;
+  if (!(negl_prob >= 0.0) || !(negl_prob < 1.0)) return BL_ERR_INVALID_ARG;
+  if (p.max_T_c > 2048) return BL_ERR_UNSUPPORTED;
+  const unsigned long long T = bl::mask_threshold(negl_prob);
+  return run_all(p, (cudaStream_t)stream, [&](const Run& r, cudaStream_t st) {
+    return bl::launch_mask(r.sh, nullptr, nullptr, tile_logw + r.mask, T, lists->mask + r.mask,
+                           lists->kv_idx + r.mask, lists->kv_cnt + r.kv_cnt,
+                           lists->q_idx + r.q_idx, lists->q_cnt + r.q_cnt, lists->nan_count,
+                           st);
+  });
+}
+
 bl_status bl_attn_bwd_varlen(const bl_varlen* varlen, const void* q, const void* k,
                              const void* v, const void* o, const void* g_o, const float* lse,
                              float scale, const bl_lists* lists, void* g_q, void* g_k,

@@ -371,6 +371,28 @@ bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_s
                                     const float* lse, double negl_prob,
                                     const bl_lists* lists, void* stream);
 
+/* Tile weights over a packed batch: bl_attn_fwd_tile_weights on every
+ * sequence.  tile_logw holds sizes.mask floats, each sequence's
+ * [H, T_r, T_c] block where its mask block is (at the same element offset).
+ * 128 x 128 tiles and at most 2048 key tiles per sequence only.  Without
+ * tile_stats the statistics rows live in `workspace` (at least
+ * bl_fwd_workspace_bytes_varlen, 16-byte aligned), whose slots every launch
+ * group of the call shares.  Two calls in flight at the same time must not
+ * share a workspace.
+ * Errors: as bl_attn_fwd_varlen; BL_ERR_UNSUPPORTED (other tile sizes, or
+ *         more than 2048 key tiles); BL_ERR_WORKSPACE. */
+size_t bl_fwd_workspace_bytes_varlen(const bl_varlen* varlen);
+bl_status bl_attn_fwd_tile_weights_varlen(const bl_varlen* varlen, const void* q, const void* k,
+                                          const void* v, float scale, void* o, float* lse,
+                                          float* tile_stats, float* tile_logw, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/* bl_mask_from_stats_varlen from the tile weights: the same lists, bit for
+ * bit, as from the statistics the weights were reduced from. */
+bl_status bl_mask_from_tile_weights_varlen(const bl_varlen* varlen, const float* tile_logw,
+                                           double negl_prob, const bl_lists* lists,
+                                           void* stream);
+
 /* bl_attn_bwd over a packed batch.  workspace: at least
  * sizes.bwd_workspace_bytes; every run has its own D and dQ areas and status
  * word in it. */

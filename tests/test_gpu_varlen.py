@@ -146,6 +146,63 @@ def test_varlen_equals_fixed_length_calls_per_sequence(name, cfg, lengths, negl)
             assert torch.equal(lists[key][s[off]:s[off] + size], l1s[key].reshape(-1)), key
 
 
+TW_CASES = [c for c in CASES if c[1]["block"] == 128] + [
+    # many launch groups on eight side streams, sharing the statistics slots
+    ("tc_d128_streams", dict(H=4, Hk=4, d=128, block=128, causal=False, window=0),
+     [900, 130, 2000, 1, 640, 640, 256, 1500], 0.05),
+]
+
+
+@pytest.mark.parametrize("name,cfg,lengths,negl", TW_CASES, ids=[c[0] for c in TW_CASES])
+def test_varlen_tile_weights_equal_the_statistics_path(name, cfg, lengths, negl):
+    """bl_attn_fwd_tile_weights_varlen leaves O, LSE and the statistics as the
+    plain packed forward writes them, its tile weights equal the fixed-length
+    call's on each sequence (with or without a statistics output), and the
+    lists built from them equal the lists built from the statistics, bit for
+    bit."""
+    from block_sparse_attention_fwd_gb300 import _lib
+    w, cu, q, k, v, go, vl = _setup(cfg, lengths, seed=6, streams=8)
+    H, bq = cfg["H"], cfg["block"]
+    scale = cfg["d"] ** -0.5
+    assert _lib.fwd_tile_weights_supported_varlen(vl)
+    qd, kd, vd, o, lse, stats = _gpu_forward(vl, q, k, v, scale)
+    z = vl.sizes
+    o1, lse1, st1 = torch.empty_like(o), torch.empty_like(lse), torch.empty_like(stats)
+    lw1 = torch.empty(z["mask"], dtype=torch.float32, device="cuda")
+    _lib.attn_fwd_tile_weights_varlen(vl, qd, kd, vd, scale, o1, lse1, lw1, tile_stats=st1)
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    lw2 = torch.full_like(lw1, float("nan"))
+    ws = torch.empty(_lib.fwd_workspace_bytes_varlen(vl), dtype=torch.uint8, device="cuda")
+    _lib.attn_fwd_tile_weights_varlen(vl, qd, kd, vd, scale, o2, lse2, lw2, workspace=ws)
+    torch.cuda.synchronize()
+    for a, b in ((o, o1), (o, o2), (lse, lse1), (lse, lse2), (stats, st1)):
+        assert torch.equal(a, b)
+    assert torch.equal(lw1.view(torch.int32), lw2.view(torch.int32))
+    seqs, _ = V.layout(cu, H, bq, bq)
+    for si, s in enumerate(seqs):
+        n = s["n"]
+        if n == 0:
+            continue
+        a = s["tok"]
+        shape = vl.seq_shape(si)
+        T_r, T_c = s["T_r"], s["T_c"]
+        q1, k1, v1 = (x[None, a:a + n].cuda() for x in (q, k, v))
+        oo = torch.empty_like(q1)
+        ll = torch.empty((1, H, n), dtype=torch.float32, device="cuda")
+        lw = torch.empty((1, H, T_r, T_c), dtype=torch.float32, device="cuda")
+        wsf = torch.empty(_lib.fwd_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+        _lib.attn_fwd_tile_weights(shape, q1, k1, v1, scale, oo, ll, lw, workspace=wsf)
+        blk = lw2[s["mask"]:s["mask"] + H * T_r * T_c]
+        assert torch.equal(blk.view(torch.int32), lw.reshape(-1).view(torch.int32)), si
+    for ng in (negl, 0.3):
+        la = _lib.alloc_varlen_lists(vl, qd.device)
+        _lib.mask_from_tile_weights_varlen(vl, lw2, ng, la)
+        lb = _lib.alloc_varlen_lists(vl, qd.device)
+        _lib.mask_from_stats_varlen(vl, stats, lse, ng, lb)
+        for key in ("mask", "kv_idx", "kv_cnt", "q_idx", "q_cnt"):
+            assert torch.equal(la[key], lb[key]), (key, ng)
+
+
 def test_varlen_corrupt_list_is_reported():
     """An out-of-range q_idx entry in one sequence's block is skipped on the
     device and reported by bl_varlen_bwd_check_status."""
