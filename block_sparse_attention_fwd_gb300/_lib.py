@@ -228,8 +228,8 @@ def attn_fwd(shape, q, k, v, scale, o, lse, tile_stats=None):
 
 def fwd_tile_weights_supported(shape: Shape) -> bool:
     """Whether bl_attn_fwd_tile_weights takes this shape (the header's rule:
-    128 x 128 tiles, head dim 64 or 128, T_c <= 2048)."""
-    return (shape.block_q == 128 and shape.block_k == 128 and shape.d in (64, 128)
+    tiles of 64 or 128, head dim 64 or 128, T_c <= 2048)."""
+    return (shape.block_q in (64, 128) and shape.block_k in (64, 128) and shape.d in (64, 128)
             and tiles(shape)[1] <= 2048)
 
 
@@ -484,11 +484,11 @@ def mask_from_stats_varlen(vl: Varlen, tile_stats, lse, negl_prob, lists):
 
 
 def fwd_tile_weights_supported_varlen(vl: Varlen) -> bool:
-    """Whether bl_attn_fwd_tile_weights_varlen takes this batch (128 x 128
-    tiles, head dim 64 or 128, at most 2048 key tiles per sequence)."""
+    """Whether bl_attn_fwd_tile_weights_varlen takes this batch (tiles of 64
+    or 128, head dim 64 or 128, at most 2048 key tiles per sequence)."""
     longest = max(b - a for a, b in zip(vl.cu_seqlens[:-1], vl.cu_seqlens[1:]))
-    return (vl.block_q == 128 and vl.block_k == 128 and vl.d in (64, 128)
-            and -(-longest // 128) <= 2048)
+    return (vl.block_q in (64, 128) and vl.block_k in (64, 128) and vl.d in (64, 128)
+            and -(-longest // vl.block_k) <= 2048)
 
 
 def fwd_workspace_bytes_varlen(vl: Varlen) -> int:

@@ -7,9 +7,9 @@ on (batch, seq_len, heads, head_dim) bf16 tensors, with key/value carrying
 ``heads_k`` heads.  With negl_prob > 0 the forward records tile statistics
 (allocating the buffer unless one is passed, README, Note) and the backward
 builds the block-sparse mask from them before running the sparse backward
-(How It Works, Phase 2).  With 128 x 128 tiles and no statistics buffer
-passed, the forward keeps only the tile weights d_ij the mask reads (the
-"Introducing BackLite" post, Using Sparsity), reduced in its epilogue.  negl_prob = 0 records nothing and runs the dense
+(How It Works, Phase 2).  With no statistics buffer passed, the forward
+keeps only the tile weights d_ij the mask reads (the "Introducing BackLite"
+post, Using Sparsity), reduced in its epilogue.  negl_prob = 0 records nothing and runs the dense
 backward (Key properties).  ``BL_VERBOSE=1`` prints mask density per head
 after each mask pass (README, Debugging, names the same kind of switch).
 ``causal=True`` (optionally with ``window=W``) gives decoder attention, with

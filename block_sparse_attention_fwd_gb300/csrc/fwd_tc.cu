@@ -375,11 +375,13 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         tmem_st16(s_col + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&x[c * 16]));
+      // rows past the statistics' T_r * block_q rows are not stored (with
+      // 64-row query tiles and an odd T_r the last 128-row MMA tile reaches
+      // 64 rows past them)
       if constexpr (SUB == 1) {
-        if (st_row)
+        if (st_row && row < sh.n_pad)
           st_row[(int64_t)j * st_stride] = row < sh.n ? (m_new + __log2f(ts)) * kLn2 : -INFINITY;
       } else {
-        // rows past the statistics' T_r * block_q rows are not stored
         if (st_row && row < sh.n_pad) {
           st_row[(int64_t)(2 * j) * st_stride] =
               row < sh.n ? (m_new + __log2f(ts_lo)) * kLn2 : -INFINITY;
@@ -458,7 +460,8 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
       gsrc = stats ? stats + bh * sh.T_c * sh.n_pad + pair * 256
                    : (s_slot >= 0 ? scr.slots + (int64_t)s_slot * scr.slot_floats : nullptr);
       gstride = stats ? sh.n_pad : kRowStride;
-      rowbytes = (stats && ntile == 1) ? 512u : 1024u;
+      // the pair's rows of a key tile: 256, fewer in the last pair
+      rowbytes = (uint32_t)min(256, (int)(sh.n_pad - pair * 256)) * 4u;
       issuer = ww == 0 && lane == 0 && gsrc != nullptr;
       fence_proxy_async_global();   // this thread's statistics, for the copies
       named_sync(1, 256);           // every row's statistics are written
@@ -503,26 +506,31 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
     }
     if (logw) {
       named_sync(1, 256);            // every row's final LSE is in s_lse
+      const int qr = sh.block_q;                        // rows per query tile
+      const int qt0 = pair * (256 / qr);                // the pair's first query tile
+      const int nq = min(256 / qr, sh.T_r - qt0);       // and how many it holds
+      const bool ranged = sh.causal || sh.window;       // (128 x 128 tiles only)
       for (int c = 0; c < nchunks; ++c) {
         const int j0 = c * JB, jn = min(JB, Tc - j0);
         const bool have = s_wissued && mbar_wait(&s_wbar[c & 1], (c >> 1) & 1);
         const float* buf = reinterpret_cast<const float*>(sm + (c & 1) * JB * (kRowStride * 4));
-        // tasks: (query tile, 32 consecutive key tiles of the chunk)
+        // tasks: (query tile, 32 consecutive key tiles of the chunk); the
+        // pair's 256 rows hold 2 query tiles of 128 rows or 4 of 64
         const int ngrp = (jn + 31) / 32;
-        for (int task = ww; task < ntile * ngrp; task += 8) {
+        for (int task = ww; task < nq * ngrp; task += 8) {
           const int tt = task / ngrp, jl = (task - tt * ngrp) * 32 + lane;
           const int j = j0 + jl;
-          const int nv = min(128, sh.n - (2 * pair + tt) * 128);   // valid rows
-          const bool in = jl < jn && j >= (tt ? lo1 : lo0) && j <= (tt ? hi1 : hi0);
-          const float* src = buf + jl * kRowStride + tt * 128;
-          const float* lp = s_lse + tt * 128;
+          const int nv = min(qr, sh.n - (qt0 + tt) * qr);   // valid rows
+          const bool in = jl < jn && (!ranged || (j >= (tt ? lo1 : lo0) && j <= (tt ? hi1 : hi0)));
+          const float* src = buf + jl * kRowStride + tt * qr;
+          const float* lp = s_lse + tt * qr;
           const float ninf = -INFINITY, qnan = __uint_as_float(0x7fc00000u);
           const float4 fill = have ? make_float4(ninf, ninf, ninf, ninf)
                                    : make_float4(qnan, qnan, qnan, qnan);
           float m0 = ninf, m1 = ninf, m2 = ninf, m3 = ninf;
-          if (nv == 128) {           // a whole tile: no row checks
+          if (nv == qr) {            // a whole tile: no row checks
 #pragma unroll 8
-            for (int r4 = 0; r4 < 128; r4 += 4) {
+            for (int r4 = 0; r4 < qr; r4 += 4) {
               const float4 v = (in && have) ? *reinterpret_cast<const float4*>(src + r4)
                                             : (in ? fill : make_float4(ninf, ninf, ninf, ninf));
               const float4 l = *reinterpret_cast<const float4*>(lp + r4);
@@ -546,7 +554,7 @@ __global__ void __launch_bounds__(384, 1) fwd_tc_kernel(
             const float mx = max_nan(max_nan(m0, m1), max_nan(m2, m3));
             float dv = isnan(mx) ? qnan : fminf(mx, 0.f);
             if (dv == 0.f) dv = 0.f;   // -0 -> +0
-            logw[(bh * sh.T_r + 2 * pair + tt) * (int64_t)Tc + j] = dv;
+            logw[(bh * sh.T_r + qt0 + tt) * (int64_t)Tc + j] = dv;
           }
         }
         named_sync(1, 256);          // every warp is done with this buffer
@@ -630,8 +638,8 @@ bool fwd_tc_supported(const Shape& sh) {
 }
 
 bool fwd_tile_weights_supported(const Shape& sh) {
-  return sh.block_q == 128 && sh.block_k == 128 && (sh.d == 64 || sh.d == 128) &&
-         sh.T_c <= 2048;
+  return (sh.block_q == 64 || sh.block_q == 128) && (sh.block_k == 64 || sh.block_k == 128) &&
+         (sh.d == 64 || sh.d == 128) && sh.T_c <= 2048;
 }
 
 size_t fwd_scratch_bytes(int d, int T_c) {
@@ -664,7 +672,6 @@ cudaError_t launch_fwd_tc(const Shape& sh, const void* q, const void* k, const v
     if (slot_tc < sh.T_c) return cudaErrorInvalidValue;
     scr.slot_floats = (int64_t)slot_tc * kRowStride;
   }
-  if (sh.block_k == 64 && logw) return cudaErrorInvalidValue;   // tile weights: 128 x 128 tiles
   auto go = [&](auto d_c, auto sub_c, auto wl_c) {
     return launch_t<decltype(d_c)::value, decltype(sub_c)::value, decltype(wl_c)::value>(
         sh, q, k, v, o, lse, stats, logw, scr, scale, zero_locks, st);

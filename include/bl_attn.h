@@ -166,7 +166,7 @@ bl_status bl_mask_from_stats(const bl_shape* shape, const float* tile_stats,
  *               no row of the tile attends (causal / window) enter with
  *               tile_stats = -inf.  This is exactly the d_ij of
  *               bl_mask_from_stats, bit for bit.
- * 128 x 128 tiles (the tcgen05 forward) and T_c <= 2048 only.
+ * Tiles of 64 or 128 on either side, T_c <= 2048.
  * ------------------------------------------------------------------------- */
 
 /* Bytes of scratch bl_attn_fwd_tile_weights needs when tile_stats is NULL:
@@ -185,9 +185,9 @@ size_t bl_fwd_workspace_bytes(const bl_shape* shape);
  *               NULL when tile_stats is given.
  * O, LSE and tile_stats are the same as bl_attn_fwd's, and tile_logw does not
  * depend on whether tile_stats is given.
- * Errors: as bl_attn_fwd; BL_ERR_UNSUPPORTED (tiles other than 128 x 128,
- *         T_c > 2048); BL_ERR_WORKSPACE (tile_stats NULL and the workspace
- *         missing or too small). */
+ * Errors: as bl_attn_fwd; BL_ERR_UNSUPPORTED (T_c > 2048);
+ *         BL_ERR_WORKSPACE (tile_stats NULL and the workspace missing or
+ *         too small). */
 bl_status bl_attn_fwd_tile_weights(const bl_shape* shape, const void* q, const void* k,
                                    const void* v, float scale, void* o, float* lse,
                                    float* tile_stats, float* tile_logw, void* workspace,
@@ -374,13 +374,13 @@ bl_status bl_mask_from_stats_varlen(const bl_varlen* varlen, const float* tile_s
 /* Tile weights over a packed batch: bl_attn_fwd_tile_weights on every
  * sequence.  tile_logw holds sizes.mask floats, each sequence's
  * [H, T_r, T_c] block where its mask block is (at the same element offset).
- * 128 x 128 tiles and at most 2048 key tiles per sequence only.  Without
+ * At most 2048 key tiles per sequence.  Without
  * tile_stats the statistics rows live in `workspace` (at least
  * bl_fwd_workspace_bytes_varlen, 16-byte aligned), whose slots every launch
  * group of the call shares.  Two calls in flight at the same time must not
  * share a workspace.
- * Errors: as bl_attn_fwd_varlen; BL_ERR_UNSUPPORTED (other tile sizes, or
- *         more than 2048 key tiles); BL_ERR_WORKSPACE. */
+ * Errors: as bl_attn_fwd_varlen; BL_ERR_UNSUPPORTED (more than 2048 key
+ *         tiles); BL_ERR_WORKSPACE. */
 size_t bl_fwd_workspace_bytes_varlen(const bl_varlen* varlen);
 bl_status bl_attn_fwd_tile_weights_varlen(const bl_varlen* varlen, const void* q, const void* k,
                                           const void* v, float scale, void* o, float* lse,

@@ -23,6 +23,10 @@ CASES = [
                    block_k=128, run=40, clusters=5, alpha=3.0), 0.05),
     (inputs.custom("mixed_n700_d64_q128k64_gqa", B=2, n=700, H=4, Hk=2, d=64, block_q=128,
                    block_k=64, run=40, clusters=5, alpha=3.0), 0.05),
+    # 64-row query tiles with an odd T_r: the last 128-row MMA tile reaches 64
+    # rows past the statistics' rows
+    (inputs.custom("mixed_n130_d128_q64k128", B=2, n=130, H=2, Hk=1, d=128, block_q=64,
+                   block_k=128, run=16, clusters=3, alpha=2.0), 0.1),
     (inputs.custom("ragged_n300_d128_t128", B=1, n=300, H=3, Hk=1, d=128, run=16,
                    clusters=4, alpha=2.0), 0.02),
     (inputs.WORKLOADS["clustered_n4096_d64"], 0.05),

@@ -28,6 +28,14 @@ CASES = [
     inputs.WORKLOADS["clustered_n4096_d64"],
     inputs.custom("tw_causal_n1500_d128", B=1, n=1500, H=4, Hk=2, d=128, run=32, clusters=8,
                   alpha=3.0, causal=True),
+    # 64-wide tiles: odd T_r (the last 128-row MMA tile reaches past the
+    # statistics' rows), both mixed shapes
+    inputs.custom("tw_q64k64_n777_d64", B=1, n=777, H=2, Hk=1, d=64, block_q=64, block_k=64,
+                  run=32, clusters=6, alpha=2.5),
+    inputs.custom("tw_q64k128_n130_d128", B=2, n=130, H=2, Hk=2, d=128, block_q=64,
+                  block_k=128, run=16, clusters=3, alpha=2.0),
+    inputs.custom("tw_q128k64_n700_d64_gqa", B=1, n=700, H=4, Hk=2, d=64, block_q=128,
+                  block_k=64, run=40, clusters=5, alpha=3.0),
     inputs.custom("tw_window_n2000_d64", B=1, n=2000, H=2, Hk=1, d=64, run=32, clusters=8,
                   alpha=3.0, causal=True, window=300),
 ]
@@ -129,8 +137,8 @@ def test_tile_weights_mask_on_planted_weights(n):
 
 def test_tile_weights_rejects_what_it_does_not_build():
     from block_sparse_attention_fwd_gb300 import _lib
-    s64 = _lib.make_shape(1, 256, 1, 1, 64, 64, 64)
-    assert _lib.fwd_workspace_bytes(s64) == 0
+    wide = _lib.make_shape(1, 2049 * 64, 1, 1, 64, 64, 64)     # T_c = 2049
+    assert _lib.fwd_workspace_bytes(wide) == 0
     big = _lib.make_shape(1, 2049 * 128, 1, 1, 128, 128, 128)    # T_c > 2048
     assert _lib.fwd_workspace_bytes(big) == 0
     s = _lib.make_shape(1, 512, 2, 1, 128, 128, 128)
