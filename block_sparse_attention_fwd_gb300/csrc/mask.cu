@@ -28,6 +28,9 @@
 // overlap another's sort.  The shared arrays are sized by a capacity CAP (the
 // smallest power of two >= T_c, at least 256); at CAP = 256 each thread holds
 // one element and the network's stages closer than a warp run on shuffles.
+// From the tile weights the forward reduced (bl_mask_from_tile_weights) the
+// d_ij come ready-made and mask_rows_warp_kernel (below) takes one warp per
+// query tile instead.
 // Kernel 2: one warp per (key tile, head, batch) compacts the mask column
 // into the ascending q list with ballots.
 #include <type_traits>
