@@ -56,8 +56,9 @@
 //               reads it transposed); after an item's last tile they write
 //               dV (warps 4-7) and s dK (warps 8-11).
 //   warps 12-15 dQ drain: thread = query row; the dQ tile goes from TMEM
-//               through a 128-byte-swizzled staging buffer into the fp32
-//               accumulator with TMA bulk reduce-adds (whole-line L2 adds).
+//               through 128-byte-swizzled staging rows into the fp32
+//               accumulator with TMA bulk reduce-adds (whole-line L2 adds),
+//               each warp its own 32 rows, 32 columns per reduce.
 // Registers: the block starts at 128 per thread; warps 0-3 give some back
 // (setmaxnreg.dec to 80) so the drain warpgroup can hold a whole 128-column
 // dQ row (setmaxnreg.inc to 176): 128*80 + 256*128 + 128*176 = 65536.  The
@@ -87,7 +88,7 @@ struct Cfg {
   static constexpr int CHUNK = 128 * 128;         // [128 rows][128 B]
   static constexpr int TILE = CHUNK * CHK;        // one 128 x d bf16 tile
   static constexpr int DS_BYTES = 2 * CHUNK;      // dS^T [128 keys][128 q] bf16
-  static constexpr int STAGE_BYTES = 128 * 128;   // dQ staging: [128 rows][32 fp32]
+  static constexpr int STAGE_BYTES = 128 * 128;   // dQ staging: 4 warps x [32 rows][32 fp32]
   static constexpr int LIST_CAP = 1536;           // cached list entries per buffer
   static constexpr int GMAX = 32;                 // heads per GQA group with cached lists
   static constexpr int OFF_K = 0;
@@ -782,10 +783,11 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
     asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
     // ------------------------------------------------------------ dQ drain
     const int q4 = warp & 3;
-    const int dt = threadIdx.x - 384;              // 0..127, = query row within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-    uint8_t* stage = sm + C::OFF_STAGE;
-    uint8_t* srow = stage + dt * 128;
+    // each warp stages its own 32 rows and issues its own reduce-adds, so the
+    // four drain warps never wait for one another between chunks
+    uint8_t* wst = sm + C::OFF_STAGE + q4 * 4096;
+    uint8_t* wrow = wst + lane * 128;
     // the four drain warps agree on success before any named barrier
     auto agree = [&](bool mine) {
       const bool w_ok = __all_sync(0xffffffffu, mine);
@@ -816,18 +818,19 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
         tmem_ld_wait();
         fence_before_sync();
         mbar_arrive(&bars.dq_free);    // R_dP is free for the next dP^T
+        const int z0 = walk.i * 128 + q4 * 32;   // this warp's first query row
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
-          if (dt == 0) bulk_wait_read0();   // previous reduce has read the staging rows
-          named_sync(1, 128);
+          if (lane == 0) bulk_wait_read0();   // the warp's previous reduce has read its rows
+          __syncwarp();
 #pragma unroll
           for (int y = 0; y < 8; ++y)
-            *reinterpret_cast<uint4*>(srow + ((y ^ (dt & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(wrow + ((y ^ (lane & 7)) << 4)) =
                 make_uint4(a[c0 + 4 * y], a[c0 + 4 * y + 1], a[c0 + 4 * y + 2], a[c0 + 4 * y + 3]);
           fence_async_smem();
-          named_sync(1, 128);
-          if (dt == 0) {
-            tma_reduce_add_4d(&tm_dq, stage, c0, walk.h, walk.i * 128, it.b);
+          __syncwarp();
+          if (lane == 0 && z0 < sh.n) {   // rows past n are dropped by the TMA unit
+            tma_reduce_add_4d(&tm_dq, wst, c0, walk.h, z0, it.b);
             bulk_commit();
           }
         }
@@ -837,7 +840,7 @@ __global__ void __launch_bounds__(512, 1) bwd_tc_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.list_empty[buf]);
     }
-    if (dt == 0) bulk_wait_read0();   // the staging rows must outlive the reads
+    if (lane == 0) bulk_wait_read0();   // the staging rows must outlive the reads
     if (!ok && lane == 0) fail();
   }
 
@@ -892,7 +895,7 @@ cudaError_t launch_t(const Shape& sh, const void* q, const void* k, const void* 
       !make_bshd_map(&mv, v, sh.B, sh.n, sh.Hk, D, 128, sh.vs) ||
       !make_bshd_map(&mgk, g_k, sh.B, sh.n, sh.Hk, D, 32, sh.ks) ||
       !make_bshd_map(&mgv, g_v, sh.B, sh.n, sh.Hk, D, 32, sh.vs) ||
-      !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 128))
+      !make_bshd_map_f32(&md, dq_acc, sh.B, sh.n, sh.H, D, 32))
     return cudaErrorInvalidValue;
   const int smem = C::BYTES + 1024;
   auto kern = bwd_tc_kernel<D, MASKED, SUB, WL>;
